@@ -1,0 +1,193 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged-KV decode attention for one GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * A paged KV cache keeps every sequence's keys and values in a pool of
+ * fixed-size physical blocks; a per-sequence block table maps logical block i
+ * (tokens [16i, 16i+16)) to a physical block, and the attention kernel gathers
+ * K/V from those non-contiguous blocks itself, with no compaction copy
+ * (Continuous-Batching-LLM-Inference-Engine README, feature list "Paged
+ * KV-cache" and "PagedAttention kernel"). The model's forward writes new K/V
+ * into the cache through slot mappings and reads them back in the paged decode
+ * attention kernel (mini-inference-engine, Connections "Llama forward -> Paged
+ * KV cache: writes and reads"; low-latency-distributed-llm-serving-
+ * infrastructure, Connections "Paged attention -> KV cache manager: maps cache
+ * slots"). The cache may be stored as INT8 (paged-inference-engine overview,
+ * "paged INT8 KV storage").
+ *
+ * Layouts (all row-major, contiguous):
+ *   k_cache, v_cache  [num_blocks, num_kv_heads, block_size, head_dim]
+ *                     one (block, kv_head) tile is one contiguous run of
+ *                     block_size*head_dim elements
+ *   k_scales, v_scales [num_blocks, num_kv_heads] fp32 (INT8 caches only)
+ *   block_tables      int32 [batch, max_blocks_per_seq]; entries past a
+ *                     sequence's ceil(len/16) blocks are not read
+ *   context_lens      int32 [batch], including the token appended this step
+ *   q, out            [batch, num_q_heads, head_dim], q's dtype
+ *   k_new, v_new      [num_tokens, num_kv_heads, head_dim]
+ *   slot_mapping      int64 [num_tokens], slot = block*block_size + row,
+ *                     negative = skip
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership and synchronisation: every pointer argument is caller-owned
+ * DEVICE memory, except the pkv_cache_desc pointer (host). The library
+ * allocates nothing and keeps no state between calls. Every call only
+ * enqueues kernels on `stream` and returns; inputs must stay valid until the
+ * stream has executed them.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a
+ * bad argument returns PKV_ERR_* and launches nothing. Conditions only the GPU
+ * can see (a block-table entry or slot outside the pool, a context length
+ * outside the table, a bounded in-kernel wait that ran out) are OR-ed as
+ * PKV_DEV_* bits into *dev_status when dev_status is non-NULL; the kernel
+ * then skips the offending work instead of touching memory outside the
+ * buffers. The library never clears *dev_status.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t; NULL = legacy default stream. */
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* NULL / misaligned pointer, bad size or shape */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, group, dtype  */
+    PKV_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than required      */
+    PKV_ERR_CUDA = 4           /* a CUDA runtime call or launch failed         */
+} pkv_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PKV_DEV_BAD_BLOCK  1u  /* block-table entry outside [0, num_blocks)    */
+#define PKV_DEV_BAD_LENGTH 2u  /* context_len < 0 or > max_blocks_per_seq*16   */
+#define PKV_DEV_BAD_SLOT   4u  /* slot >= num_blocks*block_size                */
+#define PKV_DEV_TIMEOUT    8u  /* a bounded wait on an in-kernel copy ran out  */
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
+
+/* The physical KV block pool. block_size must be 16, head_dim 64 or 128. */
+typedef struct {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    pkv_dtype kv_dtype;       /* PKV_F16, PKV_BF16 or PKV_I8 */
+} pkv_cache_desc;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *pkv_status_string(pkv_status s);
+
+/* ------------------------------------------------------------------------
+ * KV append (cache write)
+ *
+ * Writes k_new[n], v_new[n] to slot slot_mapping[n] of k_cache / v_cache for
+ * every n with slot >= 0 (the cache write that the forward pass performs each
+ * step; see the file comment). Duplicate non-negative slots in one call are a
+ * caller error.
+ *
+ * fp16 / bf16 caches: src_dtype must equal kv_dtype; the rows are stored bit
+ * for bit. k_scales, v_scales, workspace may be NULL.
+ *
+ * INT8 caches (PKV_I8): src_dtype is PKV_F16 or PKV_BF16. Codes are symmetric
+ * in [-127, 127] with one fp32 scale per (block, kv_head), K and V separately,
+ * scale = absmax/127 and round-to-nearest-even. Per (block, kv_head) tile
+ * touched by the call: a = max|x| over the call's new values in the tile,
+ * s_c = a/127 (fp32, IEEE division); with s_o the stored scale (0 = never
+ * written): s = s_c if s_o == 0; s = s_o if s_c <= s_o; otherwise s = s_c and
+ * every stored code q of the tile becomes rne((float)q * s_o / s) (fp32, left
+ * to right). New codes are clamp(rne(x / s), -127, 127), or 0 when s == 0.
+ * k_scales / v_scales must start at 0 for never-written blocks. The call needs
+ * a workspace of pkv_append_workspace_size(cache) bytes (no initial contents
+ * required; 16-byte aligned). Inputs must be finite.
+ *
+ * Alignment: k_new, v_new, k_cache, v_cache 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t pkv_append_workspace_size(const pkv_cache_desc *cache);
+
+pkv_status pkv_append(const void *k_new, const void *v_new, pkv_dtype src_dtype,
+                      int32_t num_tokens, const int64_t *slot_mapping,
+                      void *k_cache, void *v_cache, float *k_scales, float *v_scales,
+                      const pkv_cache_desc *cache, void *workspace, size_t workspace_bytes,
+                      uint32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Decode attention (one query token per sequence)
+ *
+ * out[b, h] = sum_p softmax_p(softmax_scale * <q[b,h], k_p>) * v_p over the
+ * context_lens[b] tokens of sequence b, token p read from physical block
+ * block_tables[b, p/16], row p%16 (the paged decode attention kernel of the
+ * pages; see the file comment). INT8 values dequantise as code*scale[block,
+ * kv_head]. context_lens[b] == 0 gives a zero row. Accumulation is fp32; out
+ * is rounded to q's dtype (nearest-even).
+ *
+ * Work split: the (sequence, kv_head, block) units of the whole batch are cut
+ * into num_parts equal contiguous ranges, one per worker warp (0 = one worker
+ * per resident warp slot of the device). A sequence whose blocks fall in one
+ * range is finished by that worker; the others leave fp32 partial states in
+ * the workspace that the combine step merges:
+ *   out = sum_i exp(m_i - M) o_i / sum_i exp(m_i - M) l_i,  M = max_i m_i.
+ * num_parts, batch, num_q_heads and the cache must be the same in
+ * pkv_decode_workspace_size, pkv_decode_split and pkv_decode_combine.
+ *
+ * Supported: block_size 16, head_dim 64 or 128, num_q_heads/num_kv_heads in
+ * {1, 2, 4}, 1 <= batch <= 8192; q_dtype == kv_dtype for fp16/bf16 caches,
+ * q_dtype PKV_F16 or PKV_BF16 for INT8 caches. q, out, caches 16-byte aligned;
+ * workspace 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+
+/* Resident worker warps of the split kernel on `device` (the default
+ * num_parts), or 0 if the configuration is unsupported. */
+int32_t pkv_decode_default_parts(int32_t device, int32_t batch, int32_t num_q_heads,
+                                 const pkv_cache_desc *cache);
+
+/* Workspace bytes for these sizes (num_parts 0 = the current device's
+ * default). Returns 0 for an unsupported configuration. */
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                 const pkv_cache_desc *cache, int32_t num_parts);
+
+/* Split phase and combine phase back to back on `stream`. */
+pkv_status pkv_decode_attn(const void *q, pkv_dtype q_dtype,
+                           const void *k_cache, const void *v_cache,
+                           const float *k_scales, const float *v_scales,
+                           const pkv_cache_desc *cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                           float softmax_scale, void *out,
+                           void *workspace, size_t workspace_bytes, int32_t num_parts,
+                           uint32_t *dev_status, cudaStream_t stream);
+
+/* Split phase only: each worker streams its range of KV blocks (online
+ * softmax in fp32), writes finished sequences to out and partial states
+ * (m, l, unnormalised o) to the workspace. Same arguments as pkv_decode_attn. */
+pkv_status pkv_decode_split(const void *q, pkv_dtype q_dtype,
+                            const void *k_cache, const void *v_cache,
+                            const float *k_scales, const float *v_scales,
+                            const pkv_cache_desc *cache,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                            float softmax_scale, void *out,
+                            void *workspace, size_t workspace_bytes, int32_t num_parts,
+                            uint32_t *dev_status, cudaStream_t stream);
+
+/* Combine phase (the split-K reduce): merges the partial states a preceding
+ * pkv_decode_split left in `workspace` into out, and writes zero rows for
+ * empty sequences. Must follow that split call on the same stream with the
+ * same batch, num_q_heads, cache, num_parts and workspace. */
+pkv_status pkv_decode_combine(const pkv_cache_desc *cache, int32_t batch,
+                              int32_t num_q_heads, pkv_dtype out_dtype, void *out,
+                              const void *workspace, size_t workspace_bytes,
+                              int32_t num_parts, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

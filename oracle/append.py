@@ -68,12 +68,11 @@ def append_copy(k_cache, v_cache, k_new, v_new, slot_mapping, block_size=16):
     In place, bit for bit (fp16 / bf16 caches). Negative slots are skipped.
     """
     slots = np.asarray(slot_mapping, dtype=np.int64)
-    for n, slot in enumerate(slots):
-        if slot < 0:
-            continue
-        blk, row = divmod(int(slot), block_size)
-        k_cache[blk, :, row, :] = k_new[n]
-        v_cache[blk, :, row, :] = v_new[n]
+    keep = slots >= 0
+    blk = slots[keep] // block_size
+    row = slots[keep] % block_size
+    k_cache[blk, :, row, :] = k_new[keep]
+    v_cache[blk, :, row, :] = v_new[keep]
 
 
 def _append_int8_one(cache, scales, new_f32, slots, block_size):

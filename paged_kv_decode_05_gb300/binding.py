@@ -1,0 +1,180 @@
+"""Thin ctypes binding over ``libpkv.so`` (argument marshalling only).
+
+Each function has the name of the C entry point it calls (``include/pkv.h``),
+takes torch CUDA tensors, passes their device pointers, sizes and the current
+CUDA stream, and raises :class:`PkvError` on a non-OK status. All arithmetic
+runs in the library's kernels; there is no other code path. If the library
+has not been built, loading it raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB, up_to_date
+
+PKV_F16, PKV_BF16, PKV_I8 = 0, 1, 2
+STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+          3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}
+DEV_BAD_BLOCK, DEV_BAD_LENGTH, DEV_BAD_SLOT, DEV_TIMEOUT = 1, 2, 4, 8
+BLOCK_SIZE = 16
+
+
+class PkvError(RuntimeError):
+    def __init__(self, func, code, msg):
+        super().__init__(f"{func}: {msg}")
+        self.code = code
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_DESC = ctypes.POINTER(CacheDesc)
+
+_SIGS = {
+    "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_append_workspace_size": (_SZ, [_DESC]),
+    "pkv_append": (ctypes.c_int, [_P, _P, ctypes.c_int, _I32, _P, _P, _P, _P, _P, _DESC, _P, _SZ,
+                                  _P, _P]),
+    "pkv_decode_default_parts": (_I32, [_I32, _I32, _I32, _DESC]),
+    "pkv_decode_workspace_size": (_SZ, [_I32, _I32, _DESC, _I32]),
+    "pkv_decode_attn": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
+                                       _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
+    "pkv_decode_split": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
+                                        _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
+    "pkv_decode_combine": (ctypes.c_int, [_DESC, _I32, _I32, ctypes.c_int, _P, _P, _SZ, _I32, _P]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libpkv.so`` once; raise if it is missing or older than its sources."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is not built: run paged_kv_decode_05_gb300.build.build()")
+        if not up_to_date():
+            raise RuntimeError(f"{LIB} is older than its sources: rebuild it")
+        L = ctypes.CDLL(LIB)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _check(func, code):
+    if code != 0:
+        raise PkvError(func, code, lib().pkv_status_string(code).decode())
+
+
+def _dtype_code(t):
+    import torch
+    m = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.int8: PKV_I8}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def cache_desc(k_cache) -> CacheDesc:
+    """Describe a ``[num_blocks, num_kv_heads, 16, head_dim]`` cache tensor."""
+    NB, H, bs, D = k_cache.shape
+    return CacheDesc(NB, bs, H, D, _dtype_code(k_cache))
+
+
+def pkv_status_string(code: int) -> str:
+    return lib().pkv_status_string(code).decode()
+
+
+def pkv_append_workspace_size(k_cache) -> int:
+    return int(lib().pkv_append_workspace_size(ctypes.byref(cache_desc(k_cache))))
+
+
+def pkv_append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales=None, v_scales=None,
+               workspace=None, dev_status=None, stream=None):
+    """Write ``k_new/v_new [N, Hkv, D]`` to the cache at ``slot_mapping [N] int64``."""
+    desc = cache_desc(k_cache)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().pkv_append(_ptr(k_new), _ptr(v_new), _dtype_code(k_new), int(k_new.shape[0]),
+                            _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales),
+                            _ptr(v_scales), ctypes.byref(desc), _ptr(workspace), ws_bytes,
+                            _ptr(dev_status), _stream(stream))
+    _check("pkv_append", code)
+
+
+def pkv_decode_default_parts(batch, num_q_heads, k_cache, device=None) -> int:
+    import torch
+    dev = torch.cuda.current_device() if device is None else device
+    return int(lib().pkv_decode_default_parts(dev, batch, num_q_heads,
+                                              ctypes.byref(cache_desc(k_cache))))
+
+
+def pkv_decode_workspace_size(batch, num_q_heads, k_cache, num_parts=0) -> int:
+    return int(lib().pkv_decode_workspace_size(batch, num_q_heads,
+                                               ctypes.byref(cache_desc(k_cache)), num_parts))
+
+
+def _decode(name, q, k_cache, v_cache, block_tables, context_lens, softmax_scale, out,
+            workspace, k_scales, v_scales, num_parts, dev_status, stream):
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    code = getattr(lib(), name)(
+        _ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        B, Hq, float(softmax_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(num_parts), _ptr(dev_status),
+        _stream(stream))
+    _check(name, code)
+
+
+def pkv_decode_attn(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, out,
+                    workspace, k_scales=None, v_scales=None, num_parts=0, dev_status=None,
+                    stream=None):
+    """``out [B, Hq, D] = softmax(scale q K^T) V`` over each sequence's paged KV."""
+    _decode("pkv_decode_attn", q, k_cache, v_cache, block_tables, context_lens, softmax_scale,
+            out, workspace, k_scales, v_scales, num_parts, dev_status, stream)
+
+
+def pkv_decode_split(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, out,
+                     workspace, k_scales=None, v_scales=None, num_parts=0, dev_status=None,
+                     stream=None):
+    _decode("pkv_decode_split", q, k_cache, v_cache, block_tables, context_lens, softmax_scale,
+            out, workspace, k_scales, v_scales, num_parts, dev_status, stream)
+
+
+def pkv_decode_combine(out, k_cache, workspace, num_parts=0, stream=None):
+    """Merge the partial states a preceding :func:`pkv_decode_split` left in ``workspace``."""
+    desc = cache_desc(k_cache)
+    B, Hq, D = out.shape
+    code = lib().pkv_decode_combine(ctypes.byref(desc), B, Hq, _dtype_code(out), _ptr(out),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    int(num_parts), _stream(stream))
+    _check("pkv_decode_combine", code)

@@ -1,0 +1,315 @@
+// KV append (cache write): scatter new K/V rows into the paged block pool.
+//
+// The forward pass writes each step's K/V into the paged cache through a slot
+// mapping (mini-inference-engine, Connections "Llama forward -> Paged KV
+// cache: writes and reads"; low-latency-distributed-llm-serving-infrastructure,
+// Connections "LLM engine -> KV cache manager: writes KV cache", "Paged
+// attention -> KV cache manager: maps cache slots"), optionally as INT8
+// (paged-inference-engine overview, "paged INT8 KV storage").
+//
+// fp16/bf16: one 16-byte vector per thread, a bit copy.
+// INT8: four stream-ordered kernels over (token, kv_head) warps, so that every
+// (block, kv_head) tile sees all of a call's new rows before its scale is set:
+//   clear  -> zero the tile's scratch (absmax of K, of V, owner claim)
+//   absmax -> atomicMax of each row's |x| max; atomicMax owner claim N - n
+//   scale  -> the owning warp sets the tile scale, requantising stored codes
+//             when the scale grows
+//   quant  -> every warp encodes its row with the tile's final scale
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__global__ void append_copy_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                   const int64_t* __restrict__ slots, uint4* __restrict__ k_cache,
+                                   uint4* __restrict__ v_cache, int n_tokens, int hkv,
+                                   int vec_per_row, long long pool_slots, uint32_t* status) {
+    const long long per_tok = (long long)hkv * vec_per_row;
+    const long long total = (long long)n_tokens * per_tok;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long n = i / per_tok;
+        const long long rem = i - n * per_tok;           // kvh * vec_per_row + c
+        const long long slot = slots[n];
+        if (slot < 0) continue;
+        if (slot >= pool_slots) {
+            if (rem == 0) flag_status(status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        const long long kvh = rem / vec_per_row;
+        const long long c = rem - kvh * vec_per_row;
+        const long long blk = slot / kBlockSize, row = slot % kBlockSize;
+        const long long dst = ((blk * hkv + kvh) * kBlockSize + row) * vec_per_row + c;
+        k_cache[dst] = k_new[i];
+        v_cache[dst] = v_new[i];
+    }
+}
+
+// ---------------------------------------------------------------- INT8 ---
+struct I8Args {
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slots;
+    int8_t* k_cache;
+    int8_t* v_cache;
+    float* k_scales;
+    float* v_scales;
+    uint32_t* amax_k;     // scratch [num_blocks * hkv]
+    uint32_t* amax_v;
+    uint32_t* owner;
+    uint32_t* status;
+    int n_tokens;
+    int hkv;
+    long long pool_slots;
+};
+
+// Item = (token n, kv head), one warp each. Returns the tile index or -1.
+__device__ __forceinline__ long long item_tile(const I8Args& a, long long item, long long* n_out,
+                                               int* row_out, bool flag) {
+    const long long n = item / a.hkv;
+    const int kvh = int(item - n * a.hkv);
+    const long long slot = a.slots[n];
+    *n_out = n;
+    if (slot < 0) return -1;
+    if (slot >= a.pool_slots) {
+        if (flag && kvh == 0 && (threadIdx.x & 31) == 0) flag_status(a.status, PKV_DEV_BAD_SLOT);
+        return -1;
+    }
+    *row_out = int(slot % kBlockSize);
+    return (slot / kBlockSize) * a.hkv + kvh;
+}
+
+template <typename S, int D>
+__device__ __forceinline__ void load_row(const void* src, long long row_elem0, float* x) {
+    constexpr int EPL = D / 32;  // elements per lane
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) x[e] = load_scalar(S{}, src, row_elem0 + lane * EPL + e);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+__global__ void i8_clear_kernel(I8Args a) {
+    const long long items = (long long)a.n_tokens * a.hkv;
+    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
+         it += ((long long)gridDim.x * blockDim.x) >> 5) {
+        long long n;
+        int row;
+        const long long t = item_tile(a, it, &n, &row, true);
+        if (t < 0 || (threadIdx.x & 31)) continue;
+        a.amax_k[t] = 0u;
+        a.amax_v[t] = 0u;
+        a.owner[t] = 0u;
+    }
+}
+
+template <typename S, int D>
+__global__ void i8_absmax_kernel(I8Args a) {
+    const long long items = (long long)a.n_tokens * a.hkv;
+    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
+         it += ((long long)gridDim.x * blockDim.x) >> 5) {
+        long long n;
+        int row;
+        const long long t = item_tile(a, it, &n, &row, false);
+        if (t < 0) continue;
+        float xk[D / 32], xv[D / 32];
+        load_row<S, D>(a.k_new, it * D, xk);
+        load_row<S, D>(a.v_new, it * D, xv);
+        float mk = 0.f, mv = 0.f;
+#pragma unroll
+        for (int e = 0; e < D / 32; ++e) {
+            mk = fmaxf(mk, fabsf(xk[e]));
+            mv = fmaxf(mv, fabsf(xv[e]));
+        }
+        mk = warp_max(mk);
+        mv = warp_max(mv);
+        if ((threadIdx.x & 31) == 0) {
+            // non-negative floats order like their bit patterns
+            atomicMax(&a.amax_k[t], __float_as_uint(mk));
+            atomicMax(&a.amax_v[t], __float_as_uint(mv));
+            atomicMax(&a.owner[t], uint32_t(a.n_tokens - n));
+        }
+    }
+}
+
+__device__ __forceinline__ int quant_code(float x, float s) {
+    if (s == 0.f) return 0;
+    const int q = __float2int_rn(__fdiv_rn(x, s));  // IEEE divide, ties-to-even
+    return max(-127, min(127, q));
+}
+
+// Settle one (block, kv_head) tile's scale; requantise its codes on growth.
+__device__ __forceinline__ void settle_tile(int8_t* cache, float* scales, uint32_t amax_bits,
+                                           long long t, int D) {
+    const float s_c = __fdiv_rn(__uint_as_float(amax_bits), 127.0f);
+    const float s_o = scales[t];
+    float s = s_c;
+    bool grow = false;
+    if (s_o != 0.f) {
+        if (s_c <= s_o) s = s_o;
+        else grow = true;
+    }
+    if (grow) {
+        uint32_t* words = reinterpret_cast<uint32_t*>(cache + t * kBlockSize * D);
+        const int n_words = kBlockSize * D / 4;
+        for (int w = threadIdx.x & 31; w < n_words; w += 32) {
+            const uint32_t in = words[w];
+            uint32_t out = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int q = int(int8_t(in >> (8 * b)));
+                const float r = __fdiv_rn(__fmul_rn(float(q), s_o), s);
+                out |= (uint32_t(__float2int_rn(r)) & 0xffu) << (8 * b);
+            }
+            words[w] = out;
+        }
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) scales[t] = s;
+}
+
+template <int D>
+__global__ void i8_scale_kernel(I8Args a) {
+    const long long items = (long long)a.n_tokens * a.hkv;
+    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
+         it += ((long long)gridDim.x * blockDim.x) >> 5) {
+        long long n;
+        int row;
+        const long long t = item_tile(a, it, &n, &row, false);
+        if (t < 0 || a.owner[t] != uint32_t(a.n_tokens - n)) continue;
+        settle_tile(a.k_cache, a.k_scales, a.amax_k[t], t, D);
+        settle_tile(a.v_cache, a.v_scales, a.amax_v[t], t, D);
+    }
+}
+
+template <typename S, int D>
+__global__ void i8_quant_kernel(I8Args a) {
+    constexpr int EPL = D / 32;
+    const long long items = (long long)a.n_tokens * a.hkv;
+    const int lane = threadIdx.x & 31;
+    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
+         it += ((long long)gridDim.x * blockDim.x) >> 5) {
+        long long n;
+        int row;
+        const long long t = item_tile(a, it, &n, &row, false);
+        if (t < 0) continue;
+        const long long dst = (t * kBlockSize + row) * D + lane * EPL;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            float x[EPL];
+            load_row<S, D>(kv ? a.v_new : a.k_new, it * D, x);
+            const float s = (kv ? a.v_scales : a.k_scales)[t];
+            uint32_t packed = 0;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e)
+                packed |= (uint32_t(quant_code(x[e], s)) & 0xffu) << (8 * e);
+            int8_t* cache = kv ? a.v_cache : a.k_cache;
+            if (EPL == 4) *reinterpret_cast<uint32_t*>(cache + dst) = packed;
+            else *reinterpret_cast<uint16_t*>(cache + dst) = uint16_t(packed);
+        }
+    }
+}
+
+int grid_for(long long work_items, int per_block, int cap) {
+    long long g = (work_items + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    return int(g < cap ? g : cap);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+    if (!c) return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return PKV_ERR_INVALID_ARG;
+    if (c->kv_dtype != PKV_F16 && c->kv_dtype != PKV_BF16 && c->kv_dtype != PKV_I8)
+        return PKV_ERR_INVALID_ARG;
+    if (c->block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+template <typename S, int D>
+void launch_i8(const I8Args& a, cudaStream_t st) {
+    const long long items = (long long)a.n_tokens * a.hkv;
+    const int g = grid_for(items, kWarps, 1 << 16);
+    i8_clear_kernel<<<g, kThreads, 0, st>>>(a);
+    i8_absmax_kernel<S, D><<<g, kThreads, 0, st>>>(a);
+    i8_scale_kernel<D><<<g, kThreads, 0, st>>>(a);
+    i8_quant_kernel<S, D><<<g, kThreads, 0, st>>>(a);
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t pkv_append_workspace_size(const pkv_cache_desc* cache) {
+    if (check_cache(cache) != PKV_OK) return 0;
+    if (cache->kv_dtype != PKV_I8) return 0;
+    const size_t tiles = size_t(cache->num_blocks) * size_t(cache->num_kv_heads);
+    return 3 * tiles * sizeof(uint32_t);
+}
+
+extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                                 int32_t num_tokens, const int64_t* slot_mapping, void* k_cache,
+                                 void* v_cache, float* k_scales, float* v_scales,
+                                 const pkv_cache_desc* cache, void* workspace,
+                                 size_t workspace_bytes, uint32_t* dev_status,
+                                 cudaStream_t stream) {
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    if (dev_status && !aligned(dev_status, 4)) return PKV_ERR_INVALID_ARG;
+    const int D = cache->head_dim, hkv = cache->num_kv_heads;
+    const long long pool_slots = (long long)cache->num_blocks * kBlockSize;
+
+    if (cache->kv_dtype != PKV_I8) {
+        if (src_dtype != cache->kv_dtype) return PKV_ERR_INVALID_ARG;
+        const int vpr = D * 2 / 16;
+        const long long total = (long long)num_tokens * hkv * vpr;
+        append_copy_kernel<<<grid_for(total, kThreads, 152 * 32), kThreads, 0, stream>>>(
+            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, hkv, vpr,
+            pool_slots, dev_status);
+    } else {
+        if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+        if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+            return PKV_ERR_INVALID_ARG;
+        const size_t need = pkv_append_workspace_size(cache);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PKV_ERR_WORKSPACE;
+        const size_t tiles = size_t(cache->num_blocks) * size_t(hkv);
+        uint32_t* ws = static_cast<uint32_t*>(workspace);
+        I8Args a{k_new, v_new, slot_mapping, static_cast<int8_t*>(k_cache),
+                 static_cast<int8_t*>(v_cache), k_scales, v_scales, ws, ws + tiles,
+                 ws + 2 * tiles, dev_status, num_tokens, hkv, pool_slots};
+        if (src_dtype == PKV_BF16) {
+            if (D == 128) launch_i8<BF16, 128>(a, stream); else launch_i8<BF16, 64>(a, stream);
+        } else {
+            if (D == 128) launch_i8<F16, 128>(a, stream); else launch_i8<F16, 64>(a, stream);
+        }
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG: bad pointer, size or shape";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: configuration not built";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing or too small";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA: CUDA call or launch failed";
+    }
+    return "PKV_ERR_UNKNOWN";
+}

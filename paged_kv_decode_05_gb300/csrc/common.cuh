@@ -1,0 +1,132 @@
+// Device helpers shared by the libpkv kernels: element traits, conversions
+// and thin inline-PTX wrappers for mbarriers and bulk (TMA) copies.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;      // tokens per physical block
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------- traits ---
+struct F16 {};
+struct BF16 {};
+struct I8 {};
+
+template <typename T> struct Elem;
+template <> struct Elem<F16>  { static constexpr int bytes = 2; };
+template <> struct Elem<BF16> { static constexpr int bytes = 2; };
+template <> struct Elem<I8>   { static constexpr int bytes = 1; };
+
+// ------------------------------------------------------------ conversion ---
+// Two packed 16-bit values (low half first) -> float2, exact.
+__device__ __forceinline__ float2 unpack2(BF16, uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ float2 unpack2(F16, uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+}
+// Four packed int8 codes -> four floats, exact. Each biased byte (x + 128)
+// becomes the low mantissa byte of 2^23, so the float is 2^23 + 128 + x.
+__device__ __forceinline__ void unpack4_i8(uint32_t w, float* f) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float bias = 8388736.0f;  // 2^23 + 128
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - bias;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - bias;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - bias;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - bias;
+}
+
+__device__ __forceinline__ float load_scalar(BF16, const void* p, long i) {
+    return __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p)[i]) << 16);
+}
+__device__ __forceinline__ float load_scalar(F16, const void* p, long i) {
+    return __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+__device__ __forceinline__ void store_scalar(BF16, void* p, long i, float x) {
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ void store_scalar(F16, void* p, long i, float x) {
+    reinterpret_cast<__half*>(p)[i] = __float2half_rn(x);
+}
+
+// 2^x via the SFU (ex2.approx: relative error ~2^-22; ex2(-inf) = +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------------------- mbarrier ---
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------ bulk copy ---
+// One contiguous global -> shared copy by the TMA unit; completion is
+// signalled as transaction bytes on `bar`. dst, src 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// 4-byte asynchronous global -> shared copy, tracked by cp.async groups.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void flag_status(uint32_t* st, uint32_t bits) {
+    if (st) atomicOr(st, bits);
+}
+
+}  // namespace pkv

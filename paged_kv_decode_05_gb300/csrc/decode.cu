@@ -1,0 +1,820 @@
+// Paged decode attention: split kernel (stream of KV blocks per worker warp)
+// and combine kernel (split-K reduce of partial softmax states).
+//
+// The method: one query token per sequence attends over its context, whose
+// K/V sit in fixed-size physical blocks reached through the sequence's block
+// table; the kernel gathers the blocks itself, with no compaction copy
+// (Continuous-Batching-LLM-Inference-Engine README, feature list "Paged
+// KV-cache", "PagedAttention kernel"; mini-inference-engine component "Paged
+// decode attention"; paged-inference-engine overview, "paged INT8 KV
+// storage").
+//
+// GB300 design:
+// * Work is the stream of units (sequence b, kv head, block j), ordered
+//   b-major, then kv head, then j, so each (b, kv head) "segment" is
+//   contiguous. The stream is cut into W equal ranges, one per worker warp:
+//   every warp moves the same number of bytes whatever the length mix.
+// * Each warp owns a ring of stages in shared memory. Lane 0 issues one bulk
+//   (TMA) copy for the 16-row K tile and one for the V tile of a unit (each a
+//   contiguous run of the cache), completing on the stage's mbarrier; INT8
+//   scales follow by cp.async on the same barrier. Block-table entries for the
+//   next 32 units are fetched ahead, one per lane.
+// * All g query heads of a KV head are served by the warp that reads its
+//   tiles, so each tile is read from HBM once. Scores use 8 lanes per token
+//   (q held in registers for the lane's 16 dims), packed fp32x2 FMAs and an
+//   exchange-halving shuffle reduction; the online softmax keeps a running
+//   max and sum per head in the exp2 domain; P.V gives each lane D/32
+//   output dims for all g heads.
+// * A segment that lies inside one warp's range is normalised and written
+//   out directly. Pieces of a segment that crosses ranges leave (m, l, o) in
+//   the workspace at slot (segment + worker), which is unique because both
+//   partitions are contiguous in the same order; the combine kernel merges
+//   them.
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarpsPerCta = 4;
+constexpr int kThreads = kWarpsPerCta * 32;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms when draining
+constexpr int kMaxBatch = 8192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <typename KV, int D, int G>
+struct Cfg {
+    static constexpr int esize = Elem<KV>::bytes;
+    static constexpr int kI8 = (esize == 1);
+    static constexpr int TILE = kBlockSize * D * esize;          // bytes of one K (or V) tile
+    static constexpr int ROW = D * esize;                         // bytes of one token row
+    static constexpr int STAGE = 2 * TILE;
+    static constexpr int NS = (16384 / STAGE) < 2 ? 2 : (16384 / STAGE);  // stages per warp
+    // QK mapping: 8 lanes per token row, 4 rows per pass, 4 passes.
+    static constexpr int E = D / 8;                               // elements per lane per row
+    static constexpr int VB = (E * esize) < 16 ? (E * esize) : 16;  // bytes per vector load
+    static constexpr int NV = E * esize / VB;                     // vector loads per row
+    static constexpr int EV = VB / esize;                         // elements per vector
+    // P.V mapping: each lane owns D/32 output dims.
+    static constexpr int DPL = D / 32;
+    // Exchange-halving reduction of 4*G partial dots over 8 lanes.
+    static constexpr int NVAL = 4 * G;
+    static constexpr int NF = NVAL >= 8 ? NVAL / 8 : 1;          // scores per lane afterwards
+    // Per-warp shared-memory region.
+    static constexpr int OFF_BAR = NS * STAGE;
+    static constexpr int OFF_META = OFF_BAR + NS * 8;
+    static constexpr int OFF_SCL = OFF_META + NS * 16;
+    static constexpr int OFF_P = OFF_SCL + NS * 8;
+    static constexpr int WARP_BYTES = align_up(OFF_P + kBlockSize * G * 4, 128);
+    static_assert(NS > 0 && (NS & (NS - 1)) == 0, "stage count must be a power of two");
+    static_assert(E % EV == 0 && EV % 2 == 0, "lane element layout");
+    static_assert(G == 1 || G == 2 || G == 4, "group size");
+};
+
+// Dynamic shared memory starts with 4 ints of scan scratch, then the block
+// prefix [batch + 1]; the per-warp regions follow, 128-byte aligned.
+__host__ __device__ inline int prefix_bytes(int batch) { return align_up(16 + 4 * (batch + 1), 128); }
+
+struct DecodeParams {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const float* k_scales;
+    const float* v_scales;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* out;
+    float* part_o;        // [slots, G, D]
+    float* part_ml;       // [slots, G, 2]
+    int32_t* ws_prefix;   // [batch + 1] copy of the block prefix for the combine
+    uint32_t* status;
+    int batch, hq, hkv, mb, num_blocks, workers;
+    float qscale;         // softmax_scale * log2(e)
+};
+
+__device__ __forceinline__ int clamp_len(int L, int mb, uint32_t* status, bool flag) {
+    if (L < 0 || L > mb * kBlockSize) {
+        if (flag) flag_status(status, PKV_DEV_BAD_LENGTH);
+        L = L < 0 ? 0 : mb * kBlockSize;
+    }
+    return L;
+}
+
+// prefix[b] = sum_{b' < b} ceil(L_b' / 16) for b in [0, batch]; all threads.
+__device__ void build_prefix(const DecodeParams& p, int* warp_tot, int* prefix) {
+    const int t = threadIdx.x;
+    const int chunk = (p.batch + kThreads - 1) / kThreads;
+    const int lo = min(p.batch, t * chunk), hi = min(p.batch, lo + chunk);
+    const bool flag = blockIdx.x == 0;
+    int sum = 0;
+    for (int i = lo; i < hi; ++i)
+        sum += (clamp_len(p.context_lens[i], p.mb, p.status, flag) + kBlockSize - 1) / kBlockSize;
+    // exclusive scan of per-thread sums across the CTA
+    const int lane = t & 31, warp = t >> 5;
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + inc - sum;
+    for (int i = lo; i < hi; ++i) {
+        prefix[i] = run;
+        run += (clamp_len(p.context_lens[i], p.mb, p.status, false) + kBlockSize - 1) / kBlockSize;
+    }
+    if (t == kThreads - 1) prefix[p.batch] = run;
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int i = t; i <= p.batch; i += kThreads) p.ws_prefix[i] = prefix[i];
+}
+
+// Unit u -> (b, kv head, block j): b is the last sequence whose first unit
+// is <= u (it always has blocks, since u < U).
+__device__ __forceinline__ void decode_unit(long long u, const int* prefix, int batch, int hkv,
+                                            int& b, int& kvh, int& j) {
+    const int x = int(u / hkv);
+    int lo = 0;
+    for (int step = 1 << 13; step; step >>= 1)  // kMaxBatch = 2^13
+        if (lo + step < batch && prefix[lo + step] <= x) lo += step;
+    b = lo;
+    const int nb = prefix[b + 1] - prefix[b];
+    const int r = int(u - (long long)hkv * prefix[b]);
+    kvh = r / nb;
+    j = r - kvh * nb;
+}
+
+// One exchange-halving step over lane bit `bit`: N values -> N/2 values
+// (each summed with the partner lane's), or a butterfly when N == 1.
+template <int N>
+__device__ __forceinline__ void xstep(float* v, int bit, int lane, int& base) {
+    if constexpr (N >= 2) {
+        const bool hi = (lane & bit) != 0;
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float keep = hi ? v[i + N / 2] : v[i];
+            const float send = hi ? v[i] : v[i + N / 2];
+            v[i] = keep + __shfl_xor_sync(kFull, send, bit);
+        }
+        if (hi) base += N / 2;
+    } else {
+        v[0] += __shfl_xor_sync(kFull, v[0], bit);
+    }
+}
+
+// Load NPAIR pairs of 16-bit values starting at element `off` (16-byte
+// aligned) as float2, times `scale`.
+template <typename QT, int NPAIR>
+__device__ __forceinline__ void load_q_pairs(const void* q, long long off, float scale,
+                                             float2* dst) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + off);
+#pragma unroll
+    for (int v = 0; v < NPAIR / 4; ++v) {
+        const uint4 x = __ldg(src + v);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack2(QT{}, w[i]);
+            dst[v * 4 + i] = make_float2(f.x * scale, f.y * scale);
+        }
+    }
+}
+
+// Raw words of one vector load from shared memory -> float2 pairs.
+template <typename KV, int VB>
+__device__ __forceinline__ void load_pairs_smem(const unsigned char* src, float2* dst) {
+    uint32_t w[VB / 4 > 0 ? VB / 4 : 1];
+    if constexpr (VB == 16) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src);
+        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    } else if constexpr (VB == 8) {
+        const uint2 x = *reinterpret_cast<const uint2*>(src);
+        w[0] = x.x; w[1] = x.y;
+    } else if constexpr (VB == 4) {
+        w[0] = *reinterpret_cast<const uint32_t*>(src);
+    } else {  // 2 bytes: two int8 codes
+        w[0] = *reinterpret_cast<const uint16_t*>(src);
+    }
+    if constexpr (Elem<KV>::bytes == 2) {
+#pragma unroll
+        for (int i = 0; i < VB / 4; ++i) dst[i] = unpack2(KV{}, w[i]);
+    } else {
+        constexpr int NW = VB >= 4 ? VB / 4 : 1;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            float f[4];
+            unpack4_i8(w[i], f);
+            dst[2 * i] = make_float2(f[0], f[1]);
+            if (VB >= 4) dst[2 * i + 1] = make_float2(f[2], f[3]);
+        }
+    }
+}
+
+template <typename QT, int DPL>
+__device__ __forceinline__ void store_out(void* out, long long off, const float2* v, float s) {
+    uint32_t w[DPL / 2];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) {
+        if constexpr (std::is_same<QT, BF16>::value) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[i].x * s, v[i].y * s);
+            w[i] = *reinterpret_cast<uint32_t*>(&h);
+        } else {
+            __half2 h = __floats2half2_rn(v[i].x * s, v[i].y * s);
+            w[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+    }
+    uint16_t* dst = static_cast<uint16_t*>(out) + off;
+    if constexpr (DPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else *reinterpret_cast<uint32_t*>(dst) = w[0];
+}
+
+template <typename KV, typename QT, int D, int G>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+    using C = Cfg<KV, D, G>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    int* prefix = reinterpret_cast<int*>(smem) + 4;
+    build_prefix(p, reinterpret_cast<int*>(smem), prefix);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * kWarpsPerCta + warp;
+    if (w >= p.workers) return;
+    const long long U = (long long)prefix[p.batch] * p.hkv;
+    const long long u0 = w * U / p.workers, u1 = (w + 1) * U / p.workers;
+    if (u0 >= u1) return;
+
+    unsigned char* region = smem + prefix_bytes(p.batch) + warp * C::WARP_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(region + C::OFF_BAR);
+    int4* meta = reinterpret_cast<int4*>(region + C::OFF_META);
+    float2* scl = reinterpret_cast<float2*>(region + C::OFF_SCL);
+    float* pbuf = reinterpret_cast<float*>(region + C::OFF_P);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < C::NS; ++s) mbar_init(smem_addr(&bars[s]), C::kI8 ? 2 : 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // ---- producer: block-table entries for 32 units at a time, one per lane
+    auto fetch = [&](long long base, int& b, int& kvh, int& j, int& blk) {
+        const long long u = base + lane;
+        if (u < u1) {
+            decode_unit(u, prefix, p.batch, p.hkv, b, kvh, j);
+            blk = __ldg(p.block_tables + (long long)b * p.mb + j);
+        } else {
+            b = 0; kvh = 0; j = 0; blk = -1;
+        }
+    };
+    long long cbase = u0;
+    int cb, ckvh, cj, cblk, xb, xkvh, xj, xblk;
+    fetch(cbase, cb, ckvh, cj, cblk);
+    fetch(cbase + 32, xb, xkvh, xj, xblk);
+
+    auto issue = [&](long long u, int s) {
+        int idx = int(u - cbase);
+        if (idx >= 32) {
+            cbase += 32;
+            cb = xb; ckvh = xkvh; cj = xj; cblk = xblk;
+            fetch(cbase + 32, xb, xkvh, xj, xblk);
+            idx -= 32;
+        }
+        const int b = __shfl_sync(kFull, cb, idx);
+        const int kvh = __shfl_sync(kFull, ckvh, idx);
+        const int j = __shfl_sync(kFull, cj, idx);
+        const int blk = __shfl_sync(kFull, cblk, idx);
+        if (lane == 0) {
+            const uint32_t bar = smem_addr(&bars[s]);
+            const bool ok = unsigned(blk) < unsigned(p.num_blocks);
+            meta[s] = make_int4(b, kvh, j, ok ? 1 : 0);
+            if (ok) {
+                const long long tile = (long long)blk * p.hkv + kvh;
+                unsigned char* st = region + s * C::STAGE;
+                mbar_arrive_expect_tx(bar, 2 * C::TILE);
+                bulk_g2s(smem_addr(st), static_cast<const char*>(p.k_cache) + tile * C::TILE,
+                         C::TILE, bar);
+                bulk_g2s(smem_addr(st + C::TILE),
+                         static_cast<const char*>(p.v_cache) + tile * C::TILE, C::TILE, bar);
+                if constexpr (C::kI8) {
+                    cp_async_4(smem_addr(&scl[s].x), p.k_scales + tile);
+                    cp_async_4(smem_addr(&scl[s].y), p.v_scales + tile);
+                    cp_async_arrive_noinc(bar);
+                }
+            } else {
+                flag_status(p.status, PKV_DEV_BAD_BLOCK);
+                mbar_arrive(bar);
+                if constexpr (C::kI8) mbar_arrive(bar);
+            }
+        }
+    };
+
+    // ---- consumer state: the lane's token and heads after the reduction
+    const int rgrp = lane >> 3, r8 = lane & 7;
+    int xbase = 0;
+    {
+        int n = C::NVAL;
+        for (int bit = 4; bit; bit >>= 1) {
+            if (n >= 2) {
+                if (lane & bit) xbase += n / 2;
+                n /= 2;
+            }
+        }
+    }
+    const int my_t = rgrp + 4 * (xbase / G);      // token row of the lane's scores
+    const int h0 = xbase % G;                     // first head of the lane's scores
+    const bool dup = (G == 1) && (lane & 1);      // G == 1: lane pairs hold one score
+
+    float2 q2[G][C::E / 2];
+    float m[G], lsum[C::NF];
+    float2 o2[G][C::DPL / 2];
+    int pb = -1, pkvh = -1, first_j = 0, last_j = 0, plen = 0;
+
+    auto finalize = [&]() {
+        float lh[G];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+            lh[hh] = (hh / C::NF == h0 / C::NF && !dup) ? lsum[hh % C::NF] : 0.f;
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) lh[hh] += __shfl_xor_sync(kFull, lh[hh], off);
+        const int nbk = prefix[pb + 1] - prefix[pb];
+        const long long seg = (long long)pb * p.hkv + pkvh;
+        if (first_j == 0 && last_j == nbk - 1) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
+                const long long off = ((long long)pb * p.hq + pkvh * G + h) * D + lane * C::DPL;
+                store_out<QT, C::DPL>(p.out, off, o2[h], inv);
+            }
+        } else {
+            const long long slot = seg + w;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float* dst = p.part_o + ((slot * G + h) * D + lane * C::DPL);
+                if constexpr (C::DPL == 4)
+                    *reinterpret_cast<float4*>(dst) =
+                        make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
+                else
+                    *reinterpret_cast<float2*>(dst) = o2[h][0];
+                if (lane == 0)
+                    *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) =
+                        make_float2(m[h], lh[h]);
+            }
+        }
+    };
+
+    for (int s = 0; s < C::NS; ++s)
+        if (u0 + s < u1) issue(u0 + s, s);
+    long long u_issue = (u0 + C::NS < u1) ? u0 + C::NS : u1;
+    uint32_t parity = 0;
+    long long u = u0;
+    bool aborted = false;
+    for (; u < u1; ++u) {
+        const int s = int((u - u0) & (C::NS - 1));
+        const uint32_t bar = smem_addr(&bars[s]);
+        const bool got = mbar_wait_bounded(bar, (parity >> s) & 1u, kWaitLimitNs);
+        if (!__all_sync(kFull, got)) {
+            if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+            aborted = true;
+            break;
+        }
+        parity ^= 1u << s;
+        const int4 mt = meta[s];
+        if (mt.x != pb || mt.y != pkvh) {
+            if (pb >= 0) finalize();
+            pb = mt.x;
+            pkvh = mt.y;
+            first_j = mt.z;
+            plen = clamp_len(__ldg(p.context_lens + pb), p.mb, p.status, false);
+            const long long qoff = ((long long)pb * p.hq + pkvh * G) * D;
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int c = 0; c < C::NV; ++c)
+                    load_q_pairs<QT, C::EV / 2>(p.q, qoff + h * D + c * 8 * C::EV + r8 * C::EV,
+                                                p.qscale, &q2[h][c * C::EV / 2]);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                m[h] = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < C::DPL / 2; ++i) o2[h][i] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int x = 0; x < C::NF; ++x) lsum[x] = 0.f;
+        }
+        last_j = mt.z;
+
+        if (mt.w) {
+            const unsigned char* kt = region + s * C::STAGE;
+            const unsigned char* vt = kt + C::TILE;
+            const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
+            float ksc = 1.f, vsc = 1.f;
+            if constexpr (C::kI8) {
+                const float2 sc = scl[s];
+                ksc = sc.x;
+                vsc = sc.y;
+            }
+            // scores: acc[k*G + h] = <q_h, K[rgrp + 4k]> over the lane's dims
+            float acc[C::NVAL];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const unsigned char* row = kt + (rgrp + 4 * k) * C::ROW;
+                float2 kf[C::E / 2];
+#pragma unroll
+                for (int c = 0; c < C::NV; ++c)
+                    load_pairs_smem<KV, C::VB>(row + c * 8 * C::VB + r8 * C::VB,
+                                               &kf[c * C::EV / 2]);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < C::E / 2; ++i) a = __ffma2_rn(q2[h][i], kf[i], a);
+                    acc[k * G + h] = a.x + a.y;
+                }
+            }
+            int xb = 0;
+            xstep<C::NVAL>(acc, 4, lane, xb);
+            xstep<(C::NVAL >= 2 ? C::NVAL / 2 : 1)>(acc, 2, lane, xb);
+            xstep<(C::NVAL >= 4 ? C::NVAL / 4 : 1)>(acc, 1, lane, xb);
+            float sc[C::NF];
+#pragma unroll
+            for (int x = 0; x < C::NF; ++x) sc[x] = (my_t < nv) ? acc[x] * ksc : -INFINITY;
+            // per-head block max, new running max, rescale factors
+            float bm[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+                bm[hh] = (hh / C::NF == h0 / C::NF) ? sc[hh % C::NF] : -INFINITY;
+#pragma unroll
+            for (int off = 16; off; off >>= 1)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+                    bm[hh] = fmaxf(bm[hh], __shfl_xor_sync(kFull, bm[hh], off));
+            float alpha[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float mn = fmaxf(m[hh], bm[hh]);
+                alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m[hh] - mn);
+                m[hh] = mn;
+            }
+            float pr[C::NF];
+#pragma unroll
+            for (int x = 0; x < C::NF; ++x) {
+                float mh = m[x], ah = alpha[x];
+#pragma unroll
+                for (int cand = 1; cand < G / C::NF; ++cand)
+                    if (h0 == cand * C::NF) { mh = m[cand * C::NF + x]; ah = alpha[cand * C::NF + x]; }
+                pr[x] = (sc[x] == -INFINITY) ? 0.f : fast_exp2(sc[x] - mh);
+                lsum[x] = lsum[x] * ah + pr[x];
+            }
+            if (!dup) {
+#pragma unroll
+                for (int x = 0; x < C::NF; ++x) pbuf[my_t * G + h0 + x] = pr[x] * vsc;
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int i = 0; i < C::DPL / 2; ++i)
+                    o2[h][i] = make_float2(o2[h][i].x * alpha[h], o2[h][i].y * alpha[h]);
+            __syncwarp();
+            // P.V over the valid rows of the tile
+#pragma unroll
+            for (int t = 0; t < kBlockSize; ++t) {
+                if (t < nv) {
+                    float pv[G];
+                    if constexpr (G == 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(pbuf + t * 4);
+                        pv[0] = x.x; pv[1] = x.y; pv[2] = x.z; pv[3] = x.w;
+                    } else if constexpr (G == 2) {
+                        const float2 x = *reinterpret_cast<const float2*>(pbuf + t * 2);
+                        pv[0] = x.x; pv[1] = x.y;
+                    } else {
+                        pv[0] = pbuf[t];
+                    }
+                    float2 vf[C::DPL / 2];
+                    load_pairs_smem<KV, C::DPL * C::esize>(vt + t * C::ROW + lane * C::DPL * C::esize,
+                                                          vf);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int i = 0; i < C::DPL / 2; ++i)
+                            o2[h][i] = __ffma2_rn(make_float2(pv[h], pv[h]), vf[i], o2[h][i]);
+                }
+            }
+        }
+        __syncwarp();
+        if (u_issue < u1) {
+            issue(u_issue, s);
+            ++u_issue;
+        }
+    }
+    if (!aborted) {
+        if (pb >= 0) finalize();
+        return;
+    }
+    // A copy never completed: give the others a short bounded wait, then leave.
+    for (long long v = u; v < u_issue; ++v) {
+        const int s = int((v - u0) & (C::NS - 1));
+        mbar_wait_bounded(smem_addr(&bars[s]), (parity >> s) & 1u, kDrainLimitNs);
+        parity ^= 1u << s;
+    }
+}
+
+// ---------------------------------------------------------------- combine ---
+struct CombineParams {
+    const float* part_o;
+    const float* part_ml;
+    const int32_t* ws_prefix;
+    void* out;
+    int batch, hq, hkv, workers;
+};
+
+// Worker whose range holds unit u: the largest w with floor(w*U/W) <= u.
+__device__ __forceinline__ long long worker_of(long long u, long long U, long long W) {
+    return ((u + 1) * W - 1) / U;
+}
+
+// With fewer units than workers some ranges are empty; they write nothing.
+__device__ __forceinline__ bool worker_nonempty(long long w, long long U, long long W) {
+    return w * U / W < (w + 1) * U / W;
+}
+
+// One CTA per segment (sequence b, kv head): merge the pieces' states
+// out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i (scores are in log2
+// units), or write zeros for an empty sequence. Segments finished inside one
+// worker were written by the split kernel and are skipped.
+template <typename QT, int D, int G>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const CombineParams c) {
+    const int seg = blockIdx.x;
+    const int b = seg / c.hkv, kvh = seg - b * c.hkv;
+    const int* P = c.ws_prefix;
+    const int nb = P[b + 1] - P[b];
+    constexpr int Q = D / 4;
+    const long long obase = ((long long)b * c.hq + kvh * G) * D;
+    if (nb == 0) {
+        for (int it = threadIdx.x; it < G * Q; it += blockDim.x) {
+            const float2 z[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            store_out<QT, 4>(c.out, obase + (long long)it * 4, z, 0.f);
+        }
+        return;
+    }
+    const long long U = (long long)P[c.batch] * c.hkv;
+    const long long uf = (long long)c.hkv * P[b] + (long long)kvh * nb;
+    const long long wf = worker_of(uf, U, c.workers), wl = worker_of(uf + nb - 1, U, c.workers);
+    if (wf == wl) return;
+    for (int it = threadIdx.x; it < G * Q; it += blockDim.x) {
+        const int h = it / Q, d4 = it - h * Q;
+        float M = -INFINITY;
+        for (long long w = wf; w <= wl; ++w)
+            if (worker_nonempty(w, U, c.workers)) M = fmaxf(M, c.part_ml[((seg + w) * G + h) * 2]);
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (long long w = wf; w <= wl; ++w) {
+            if (!worker_nonempty(w, U, c.workers)) continue;  // wrote no piece
+            const long long slot = seg + w;
+            const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + (slot * G + h) * 2);
+            const float a = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+            const float4 o = *reinterpret_cast<const float4*>(c.part_o + (slot * G + h) * D + d4 * 4);
+            den += a * ml.y;
+            num.x += a * o.x; num.y += a * o.y; num.z += a * o.z; num.w += a * o.w;
+        }
+        const float inv = den > 0.f ? 1.0f / den : 0.f;
+        const float2 v[2] = {make_float2(num.x, num.y), make_float2(num.z, num.w)};
+        store_out<QT, 4>(c.out, obase + (long long)h * D + d4 * 4, v, inv);
+    }
+}
+
+// ------------------------------------------------------------------- host ---
+struct Ops {
+    int warp_bytes;
+    cudaError_t (*prepare)(size_t smem);                        // smem attribute
+    cudaError_t (*occupancy)(int* blocks, size_t smem);
+    void (*split)(const DecodeParams&, int grid, size_t smem, cudaStream_t);
+    void (*combine)(const CombineParams&, int grid, cudaStream_t);
+};
+
+template <typename KV, typename QT, int D, int G>
+struct Impl {
+    static cudaError_t prepare(size_t smem) {
+        return cudaFuncSetAttribute(decode_split_kernel<KV, QT, D, G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    }
+    static cudaError_t occupancy(int* blocks, size_t smem) {
+        cudaError_t e = prepare(smem);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            blocks, decode_split_kernel<KV, QT, D, G>, kThreads, smem);
+    }
+    static void split(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
+        decode_split_kernel<KV, QT, D, G><<<grid, kThreads, smem, st>>>(p);
+    }
+    static void combine(const CombineParams& c, int grid, cudaStream_t st) {
+        decode_combine_kernel<QT, D, G><<<grid, 128, 0, st>>>(c);
+    }
+    static Ops ops() { return Ops{Cfg<KV, D, G>::WARP_BYTES, prepare, occupancy, split, combine}; }
+};
+
+template <typename KV, typename QT, int D>
+bool pick_g(int G, Ops* o) {
+    switch (G) {
+        case 1: *o = Impl<KV, QT, D, 1>::ops(); return true;
+        case 2: *o = Impl<KV, QT, D, 2>::ops(); return true;
+        case 4: *o = Impl<KV, QT, D, 4>::ops(); return true;
+    }
+    return false;
+}
+
+template <typename KV, typename QT>
+bool pick_d(int D, int G, Ops* o) {
+    if (D == 128) return pick_g<KV, QT, 128>(G, o);
+    if (D == 64) return pick_g<KV, QT, 64>(G, o);
+    return false;
+}
+
+bool pick_ops(pkv_dtype kv, pkv_dtype q, int D, int G, Ops* o) {
+    if (kv == PKV_BF16 && q == PKV_BF16) return pick_d<BF16, BF16>(D, G, o);
+    if (kv == PKV_F16 && q == PKV_F16) return pick_d<F16, F16>(D, G, o);
+    if (kv == PKV_I8 && q == PKV_BF16) return pick_d<I8, BF16>(D, G, o);
+    if (kv == PKV_I8 && q == PKV_F16) return pick_d<I8, F16>(D, G, o);
+    return false;
+}
+
+struct Layout {
+    size_t prefix_off, ml_off, o_off, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout layout(int batch, int hkv, int G, int D, long long workers) {
+    const long long slots = (long long)batch * hkv + workers;
+    Layout l;
+    l.prefix_off = 0;
+    l.ml_off = align256(sizeof(int32_t) * size_t(batch + 1));
+    l.o_off = l.ml_off + align256(size_t(slots) * G * 2 * sizeof(float));
+    l.total = l.o_off + align256(size_t(slots) * G * D * sizeof(float));
+    return l;
+}
+
+bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks shared by every decode entry point; fills ops and the group size.
+pkv_status check_decode(const pkv_cache_desc* c, int batch, int hq, pkv_dtype q_dtype, Ops* ops,
+                        int* G) {
+    if (!c) return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return PKV_ERR_INVALID_ARG;
+    if (c->kv_dtype != PKV_F16 && c->kv_dtype != PKV_BF16 && c->kv_dtype != PKV_I8)
+        return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (batch < 0 || hq <= 0 || hq % c->num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (c->block_size != kBlockSize || batch > kMaxBatch) return PKV_ERR_UNSUPPORTED;
+    if (c->kv_dtype != PKV_I8 && q_dtype != c->kv_dtype) return PKV_ERR_INVALID_ARG;
+    *G = hq / c->num_kv_heads;
+    if (!pick_ops(c->kv_dtype, q_dtype, c->head_dim, *G, ops)) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+size_t split_smem(const Ops& o, int batch) {
+    return size_t(prefix_bytes(batch)) + size_t(kWarpsPerCta) * o.warp_bytes;
+}
+
+// Resident worker warps on the current device for this configuration.
+long long default_workers(const Ops& o, int batch) {
+    int dev = 0, sms = 0, blocks = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (o.occupancy(&blocks, split_smem(o, batch)) != cudaSuccess || blocks <= 0) return 0;
+    return (long long)sms * blocks * kWarpsPerCta;
+}
+
+pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q_dtype,
+                      const void* k_cache, const void* v_cache, const float* k_scales,
+                      const float* v_scales, const pkv_cache_desc* cache,
+                      const int32_t* block_tables, int32_t mb, const int32_t* context_lens,
+                      int32_t batch, int32_t hq, float softmax_scale, void* out, void* workspace,
+                      size_t workspace_bytes, int32_t num_parts, uint32_t* dev_status,
+                      cudaStream_t stream) {
+    Ops ops;
+    int G = 0;
+    pkv_status s = check_decode(cache, batch, hq, q_dtype, &ops, &G);
+    if (s != PKV_OK) return s;
+    if (batch == 0) return PKV_OK;
+    if (num_parts < 0) return PKV_ERR_INVALID_ARG;
+    if (!out || !is_aligned(out, 16)) return PKV_ERR_INVALID_ARG;
+    if (do_split) {
+        if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+        if (!is_aligned(q, 16) || !is_aligned(k_cache, 16) || !is_aligned(v_cache, 16) ||
+            !is_aligned(block_tables, 4) || !is_aligned(context_lens, 4))
+            return PKV_ERR_INVALID_ARG;
+        if (cache->kv_dtype == PKV_I8 && (!k_scales || !v_scales || !is_aligned(k_scales, 4) ||
+                                          !is_aligned(v_scales, 4)))
+            return PKV_ERR_INVALID_ARG;
+        if (mb <= 0 || !(softmax_scale == softmax_scale) || softmax_scale > 3.0e38f ||
+            softmax_scale < -3.0e38f)
+            return PKV_ERR_INVALID_ARG;
+        if (dev_status && !is_aligned(dev_status, 4)) return PKV_ERR_INVALID_ARG;
+    }
+    const long long workers = num_parts > 0 ? num_parts : default_workers(ops, batch);
+    if (workers <= 0) return PKV_ERR_CUDA;
+    const int D = cache->head_dim, hkv = cache->num_kv_heads;
+    const Layout l = layout(batch, hkv, G, D, workers);
+    if (!workspace || workspace_bytes < l.total || !is_aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    if (do_split) {
+        const size_t smem = split_smem(ops, batch);
+        if (ops.prepare(smem) != cudaSuccess) return PKV_ERR_CUDA;
+        DecodeParams p;
+        p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
+        p.k_scales = k_scales; p.v_scales = v_scales;
+        p.block_tables = block_tables; p.context_lens = context_lens; p.out = out;
+        p.part_o = reinterpret_cast<float*>(ws + l.o_off);
+        p.part_ml = reinterpret_cast<float*>(ws + l.ml_off);
+        p.ws_prefix = reinterpret_cast<int32_t*>(ws + l.prefix_off);
+        p.status = dev_status;
+        p.batch = batch; p.hq = hq; p.hkv = hkv; p.mb = mb; p.num_blocks = cache->num_blocks;
+        p.workers = int(workers);
+        p.qscale = softmax_scale * kLog2e;
+        const int grid = int((workers + kWarpsPerCta - 1) / kWarpsPerCta);
+        ops.split(p, grid, smem, stream);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    if (do_combine) {
+        CombineParams c;
+        c.part_o = reinterpret_cast<const float*>(ws + l.o_off);
+        c.part_ml = reinterpret_cast<const float*>(ws + l.ml_off);
+        c.ws_prefix = reinterpret_cast<const int32_t*>(ws + l.prefix_off);
+        c.out = out;
+        c.batch = batch; c.hq = hq; c.hkv = hkv; c.workers = int(workers);
+        ops.combine(c, batch * hkv, stream);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int32_t pkv_decode_default_parts(int32_t device, int32_t batch, int32_t num_q_heads,
+                                            const pkv_cache_desc* cache) {
+    Ops ops;
+    int G = 0;
+    const pkv_dtype qd = (cache && cache->kv_dtype == PKV_F16) ? PKV_F16 : PKV_BF16;
+    if (check_decode(cache, batch, num_q_heads, qd, &ops, &G) != PKV_OK) return 0;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return 0;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return 0;
+    const long long w = default_workers(ops, batch < 1 ? 1 : batch);
+    if (prev != device) cudaSetDevice(prev);
+    return int32_t(w);
+}
+
+extern "C" size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                            const pkv_cache_desc* cache, int32_t num_parts) {
+    Ops ops;
+    int G = 0;
+    const pkv_dtype qd = (cache && cache->kv_dtype == PKV_F16) ? PKV_F16 : PKV_BF16;
+    if (check_decode(cache, batch, num_q_heads, qd, &ops, &G) != PKV_OK || num_parts < 0) return 0;
+    const long long workers = num_parts > 0 ? num_parts : default_workers(ops, batch < 1 ? 1 : batch);
+    if (workers <= 0) return 0;
+    return layout(batch, cache->num_kv_heads, G, cache->head_dim, workers).total;
+}
+
+extern "C" pkv_status pkv_decode_attn(const void* q, pkv_dtype q_dtype, const void* k_cache,
+                                      const void* v_cache, const float* k_scales,
+                                      const float* v_scales, const pkv_cache_desc* cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t batch,
+                                      int32_t num_q_heads, float softmax_scale, void* out,
+                                      void* workspace, size_t workspace_bytes, int32_t num_parts,
+                                      uint32_t* dev_status, cudaStream_t stream) {
+    return run_decode(true, true, q, q_dtype, k_cache, v_cache, k_scales, v_scales, cache,
+                      block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                      softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream);
+}
+
+extern "C" pkv_status pkv_decode_split(const void* q, pkv_dtype q_dtype, const void* k_cache,
+                                       const void* v_cache, const float* k_scales,
+                                       const float* v_scales, const pkv_cache_desc* cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t batch,
+                                       int32_t num_q_heads, float softmax_scale, void* out,
+                                       void* workspace, size_t workspace_bytes, int32_t num_parts,
+                                       uint32_t* dev_status, cudaStream_t stream) {
+    return run_decode(true, false, q, q_dtype, k_cache, v_cache, k_scales, v_scales, cache,
+                      block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                      softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream);
+}
+
+extern "C" pkv_status pkv_decode_combine(const pkv_cache_desc* cache, int32_t batch,
+                                         int32_t num_q_heads, pkv_dtype out_dtype, void* out,
+                                         const void* workspace, size_t workspace_bytes,
+                                         int32_t num_parts, cudaStream_t stream) {
+    return run_decode(false, true, nullptr, out_dtype, nullptr, nullptr, nullptr, nullptr, cache,
+                      nullptr, 0, nullptr, batch, num_q_heads, 1.0f, out,
+                      const_cast<void*>(workspace), workspace_bytes, num_parts, nullptr, stream);
+}
