@@ -1,0 +1,468 @@
+"""Benchmark: one decode step of paged-KV attention on GB300.
+
+A step is the whole hot path for one batch: append the step's new K/V token
+per sequence into the paged cache (pkv_append), then paged decode attention
+(pkv_decode_split + pkv_decode_combine). Default workload: the GQA
+Llama-3-8B-shape batch (B=256, 32 q / 8 kv heads, D=128, bf16, L~U[128,4096]).
+
+    python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
+
+Prints one JSON line. `value` is the decode-attention HBM throughput of the
+whole step: algorithmic bytes (KV + q + block tables, per the workload) over
+the step time, summed over ranks. The KV cache (2.2 GB) is far larger than L2,
+so no flush is needed between steps. `--impl reference` times the CPU oracle
+(float64 NumPy) on the host cores over a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_decode_05_gb300.workloads import (CONFIGS, DESCRIPTIONS,  # noqa: E402
+                                                algorithmic_bytes, make_workload)
+
+METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak) and decode tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", default="gqa8b", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--num-parts", type=int, default=0, help="worker warps (0 = device default)")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    """HBM roofline denominator: the measured copy bandwidth if present."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel: str, config: str):
+    """DRAM bytes per launch from the committed ncu summary, if still current.
+
+    profiles/<kernel>_<config>.md carries a line
+    ``traffic_bytes_per_launch: N source_sha256: H``; it counts only while H
+    matches the current kernel source.
+    """
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
+    src = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc", "decode.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            if line.startswith("traffic_bytes_per_launch:"):
+                parts = line.split()
+                if parts[3] == h:
+                    return int(parts[1])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, n = [], None, set(), 0
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), f[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def oracle_sample(w, budget_s: float, first: int = 0):
+    """Time the CPU oracle on whole sequences until ~budget_s (at least one).
+
+    Returns (seconds, algorithmic bytes covered, sequences, threads).
+    """
+    import oracle
+    cfg = w.cfg
+    shape = (w.num_blocks, cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    if cfg.kv_dtype == "i8":
+        k = np.zeros(shape, np.int8); v = np.zeros(shape, np.int8)
+        ks = np.zeros(shape[:2], np.float32); vs = np.zeros(shape[:2], np.float32)
+        oracle.append_int8(k, v, ks, vs, w.k_fill, w.v_fill, w.fill_slots)
+        oracle.append_int8(k, v, ks, vs, w.k_step, w.v_step, w.step_slots)
+    else:
+        dt = np.uint16 if cfg.kv_dtype == "bf16" else np.float16
+        k = np.zeros(shape, dt); v = np.zeros(shape, dt); ks = vs = None
+        oracle.append_copy(k, v, w.k_fill, w.v_fill, w.fill_slots)
+        oracle.append_copy(k, v, w.k_step, w.v_step, w.step_slots)
+    seqs, t_total = [], 0.0
+    b = first
+    while len(seqs) < cfg.batch and (t_total < budget_s or not seqs):
+        t0 = time.perf_counter()
+        oracle.paged_decode_attention(w.q, k, v, w.block_tables, w.context_lens,
+                                      cfg.softmax_scale, ks, vs, seqs=[b])
+        t_total += time.perf_counter() - t0
+        seqs.append(b)
+        b = (b + 1) % cfg.batch
+    lens = w.context_lens[seqs]
+    from paged_kv_decode_05_gb300.workloads import variant
+    byts = algorithmic_bytes(variant(cfg, batch=len(seqs)), lens)
+    return t_total, byts, seqs, _threads()
+
+
+def _threads() -> int:
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 1) for d in threadpool_info()]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def _gpu_state(w, device):
+    """Device tensors for one workload: cache filled by pkv_append, step inputs."""
+    import torch
+    from paged_kv_decode_05_gb300 import binding as B
+    cfg = w.cfg
+
+    def dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    shape = (w.num_blocks, cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    st = {"status": torch.zeros(1, dtype=torch.int32, device=device)}
+    if cfg.kv_dtype == "i8":
+        st["k_cache"] = torch.zeros(shape, dtype=torch.int8, device=device)
+        st["v_cache"] = torch.zeros(shape, dtype=torch.int8, device=device)
+        st["k_scales"] = torch.zeros(shape[:2], dtype=torch.float32, device=device)
+        st["v_scales"] = torch.zeros(shape[:2], dtype=torch.float32, device=device)
+        n = B.pkv_append_workspace_size(st["k_cache"])
+        st["append_ws"] = torch.empty(n, dtype=torch.uint8, device=device)
+    else:
+        dt = torch.bfloat16 if cfg.kv_dtype == "bf16" else torch.float16
+        st["k_cache"] = torch.zeros(shape, dtype=dt, device=device)
+        st["v_cache"] = torch.zeros(shape, dtype=dt, device=device)
+        st["k_scales"] = st["v_scales"] = st["append_ws"] = None
+    B.pkv_append(dev(w.k_fill), dev(w.v_fill), dev(w.fill_slots), st["k_cache"], st["v_cache"],
+                 st["k_scales"], st["v_scales"], st["append_ws"], st["status"])
+    st["q"] = dev(w.q)
+    st["k_step"], st["v_step"] = dev(w.k_step), dev(w.v_step)
+    st["step_slots"] = dev(w.step_slots)
+    st["block_tables"], st["context_lens"] = dev(w.block_tables), dev(w.context_lens)
+    st["out"] = torch.empty_like(st["q"])
+    torch.cuda.synchronize(device)
+    return st
+
+
+def _step(st, cfg, ws, parts, ev=None):
+    """One decode step: append the new token, split, combine (3 or 6 launches)."""
+    from paged_kv_decode_05_gb300 import binding as B
+    B.pkv_append(st["k_step"], st["v_step"], st["step_slots"], st["k_cache"], st["v_cache"],
+                 st["k_scales"], st["v_scales"], st["append_ws"], st["status"])
+    if ev is not None:
+        ev[0].record()
+    B.pkv_decode_split(st["q"], st["k_cache"], st["v_cache"], st["block_tables"],
+                       st["context_lens"], cfg.softmax_scale, st["out"], ws, st["k_scales"],
+                       st["v_scales"], parts, st["status"])
+    if ev is not None:
+        ev[1].record()
+    B.pkv_decode_combine(st["out"], st["k_cache"], ws, parts)
+
+
+def run_native(args):
+    import torch
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_decode_05_gb300 import binding as B
+    from paged_kv_decode_05_gb300.build import build
+    if rank == 0:
+        build()
+    barrier(world, device)
+    B.lib()
+
+    cfg = CONFIGS[args.config]
+    w = make_workload(cfg, seed=cfg.seed + rank)   # one replica per rank (weak scaling)
+    st = _gpu_state(w, device)
+    parts = args.num_parts or B.pkv_decode_default_parts(cfg.batch, cfg.num_q_heads,
+                                                         st["k_cache"], device.index)
+    ws = torch.empty(B.pkv_decode_workspace_size(cfg.batch, cfg.num_q_heads, st["k_cache"], parts),
+                     dtype=torch.uint8, device=device)
+    alg = algorithmic_bytes(cfg, w.context_lens)
+    launches_per_step = 6 if cfg.kv_dtype == "i8" else 3
+    K, W = args.steps, args.warmup
+
+    for _ in range(W):
+        _step(st, cfg, ws, parts)
+    torch.cuda.synchronize(device)
+
+    # ---- device-timed region: K steps, inputs resident in HBM
+    split_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(str(getattr(props, "uuid", local)).strip())
+    if str(sampler.gpu_id) and not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + sampler.gpu_id
+    sampler.start()
+    time.sleep(0.5)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    wall0 = time.time()
+    t_start.record()
+    for i in range(K):
+        _step(st, cfg, ws, parts, split_ev[i])
+    t_end.record()
+    torch.cuda.synchronize(device)
+    wall1 = time.time()
+    barrier(world, device)
+    time.sleep(0.2)
+    clocks = sampler.stop(wall0, wall1)
+    ms_total = reduce_max(t_start.elapsed_time(t_end), world, device)
+    split_ms = [a.elapsed_time(b) for a, b in split_ev]
+    split_avg_ms = sum(split_ms) / len(split_ms)
+    status = int(st["status"].item())
+
+    # ---- end-to-end through the C ABI with host buffers (H2D inputs, D2H output)
+    e2e = _e2e(st, w, cfg, ws, parts, device, min(K, args.e2e_steps), world)
+
+    step_s = ms_total / 1e3 / K
+    value = alg * world / step_s / 1e9
+    peak, peak_src = load_peaks()
+    achieved = alg / (split_avg_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_total / K, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.kv_dtype, "data": "synthetic (seeded N(0,1) K/V/q, shuffled block pool)",
+        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+                   "batch": cfg.batch, "num_q_heads": cfg.num_q_heads,
+                   "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+                   "block_size": cfg.block_size, "total_context_tokens": w.total_tokens,
+                   "algorithmic_bytes_per_step": alg, "workers": parts,
+                   "l2": "no flush: the KV cache read each step (%.2f GB) is far larger than "
+                         "the 129 MB L2" % (alg / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / world / peak, 2),
+        "decode_tokens_per_s": round(cfg.batch * world / step_s, 1),
+        "kv_tokens_per_s": round(w.total_tokens * world / step_s, 1),
+        "roofline": {"kernel": "decode_split_kernel", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("decode_split_kernel", args.config),
+                     "split_ms_avg": round(split_avg_ms, 6)},
+        "e2e": e2e, "gpu_launches": K * launches_per_step, "clocks": clocks,
+        "device_status": status,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        t, byts, seqs, thr = oracle_sample(w, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": round(byts / t / 1e9, 4), "unit": "GB/s", "cores": thr,
+                                "kind": "oracle",
+                                "sample": f"float64 oracle attention over {len(seqs)} of "
+                                          f"{cfg.batch} sequences ({t:.1f} s), same workload"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _e2e(st, w, cfg, ws, parts, device, K, world):
+    """Same metric through the C ABI, with the step's inputs copied from pinned
+    host memory and the output copied back inside the timed region."""
+    import torch
+    names = ["q", "k_step", "v_step", "step_slots", "block_tables", "context_lens"]
+    host = {n: st[n].cpu().pin_memory() for n in names}
+    out_host = torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_host.numel() * out_host.element_size()
+    for _ in range(3):
+        for n in names:
+            st[n].copy_(host[n], non_blocking=True)
+        _step(st, cfg, ws, parts)
+        out_host.copy_(st["out"], non_blocking=True)
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        for n in names:
+            st[n].copy_(host[n], non_blocking=True)
+        _step(st, cfg, ws, parts)
+        out_host.copy_(st["out"], non_blocking=True)
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = reduce_max(a.elapsed_time(b), world, device)
+    alg = algorithmic_bytes(cfg, w.context_lens)
+    return {"value": round(alg * world / (ms / 1e3 / K) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K,
+            "ms_per_step": round(ms / K, 6)}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the oracle's decode of
+    one sequence of the workload (cycling through the batch), on host cores."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.config]
+    w = make_workload(cfg)
+    # one oracle-built cache, then K timed steps of one sequence each
+    import oracle
+    shape = (w.num_blocks, cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    if cfg.kv_dtype == "i8":
+        k = np.zeros(shape, np.int8); v = np.zeros(shape, np.int8)
+        ks = np.zeros(shape[:2], np.float32); vs = np.zeros(shape[:2], np.float32)
+        oracle.append_int8(k, v, ks, vs, w.k_fill, w.v_fill, w.fill_slots)
+        oracle.append_int8(k, v, ks, vs, w.k_step, w.v_step, w.step_slots)
+    else:
+        dt = np.uint16 if cfg.kv_dtype == "bf16" else np.float16
+        k = np.zeros(shape, dt); v = np.zeros(shape, dt); ks = vs = None
+        oracle.append_copy(k, v, w.k_fill, w.v_fill, w.fill_slots)
+        oracle.append_copy(k, v, w.k_step, w.v_step, w.step_slots)
+    from paged_kv_decode_05_gb300.workloads import variant
+
+    def one(b):
+        oracle.paged_decode_attention(w.q, k, v, w.block_tables, w.context_lens,
+                                      cfg.softmax_scale, ks, vs, seqs=[b])
+
+    for i in range(args.warmup):
+        one(i % cfg.batch)
+    seqs = [(args.warmup + i) % cfg.batch for i in range(args.steps)]
+    t0 = time.perf_counter()
+    for b in seqs:
+        one(b)
+    t = time.perf_counter() - t0
+    byts = algorithmic_bytes(variant(cfg, batch=len(seqs)), w.context_lens[seqs])
+    value = byts / t / 1e9
+    cores = _threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+                   "step": "oracle decode of one sequence of the batch, cycling"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{len(seqs)} single-sequence float64 oracle decodes "
+                                   f"({t:.1f} s)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()
