@@ -255,18 +255,26 @@ def _gpu_state(w, device):
 
 
 def _step(st, cfg, ws, parts, ev=None):
-    """One decode step: append the new token, split, combine (3 or 6 launches)."""
+    """One decode step: append the new token, split, combine (3 or 6 launches).
+
+    ``ev``: optional 4 CUDA events recorded before the append, between append
+    and split, between split and combine, and after the combine.
+    """
     from paged_kv_decode_05_gb300 import binding as B
+    if ev is not None:
+        ev[0].record()
     B.pkv_append(st["k_step"], st["v_step"], st["step_slots"], st["k_cache"], st["v_cache"],
                  st["k_scales"], st["v_scales"], st["append_ws"], st["status"])
     if ev is not None:
-        ev[0].record()
+        ev[1].record()
     B.pkv_decode_split(st["q"], st["k_cache"], st["v_cache"], st["block_tables"],
                        st["context_lens"], cfg.softmax_scale, st["out"], ws, st["k_scales"],
                        st["v_scales"], parts, st["status"])
     if ev is not None:
-        ev[1].record()
+        ev[2].record()
     B.pkv_decode_combine(st["out"], st["k_cache"], ws, parts)
+    if ev is not None:
+        ev[3].record()
 
 
 def run_native(args):
@@ -300,8 +308,7 @@ def run_native(args):
     torch.cuda.synchronize(device)
 
     # ---- device-timed region: K steps, inputs resident in HBM
-    split_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(K)]
+    step_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(device)
     sampler = ClockSampler(str(getattr(props, "uuid", local)).strip())
@@ -314,7 +321,7 @@ def run_native(args):
     wall0 = time.time()
     t_start.record()
     for i in range(K):
-        _step(st, cfg, ws, parts, split_ev[i])
+        _step(st, cfg, ws, parts, step_ev[i])
     t_end.record()
     torch.cuda.synchronize(device)
     wall1 = time.time()
@@ -322,8 +329,8 @@ def run_native(args):
     time.sleep(0.2)
     clocks = sampler.stop(wall0, wall1)
     ms_total = reduce_max(t_start.elapsed_time(t_end), world, device)
-    split_ms = [a.elapsed_time(b) for a, b in split_ev]
-    split_avg_ms = sum(split_ms) / len(split_ms)
+    avg = lambda i, j: sum(e[i].elapsed_time(e[j]) for e in step_ev) / K  # noqa: E731
+    append_avg_ms, split_avg_ms, combine_avg_ms = avg(0, 1), avg(1, 2), avg(2, 3)
     status = int(st["status"].item())
 
     # ---- end-to-end through the C ABI with host buffers (H2D inputs, D2H output)
@@ -355,6 +362,8 @@ def run_native(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic("decode_split_kernel", args.config),
                      "split_ms_avg": round(split_avg_ms, 6)},
+        "kernel_ms_avg": {"append": round(append_avg_ms, 6), "split": round(split_avg_ms, 6),
+                          "combine": round(combine_avg_ms, 6)},
         "e2e": e2e, "gpu_launches": K * launches_per_step, "clocks": clocks,
         "device_status": status,
     }
