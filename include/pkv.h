@@ -186,6 +186,44 @@ pkv_status pkv_decode_combine(const pkv_cache_desc *cache, int32_t batch,
                               const void *workspace, size_t workspace_bytes,
                               int32_t num_parts, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Decode attention without any allocation by anyone
+ *
+ * No counterpart on the source pages: this variant exists for callers that
+ * cannot call cudaMalloc. Some runtimes plan all device memory ahead of time
+ * and own the allocator, so a library may not take memory of its own; on a
+ * latency-critical serving loop an allocation (and the device-wide
+ * synchronisation a cudaFree brings) is not acceptable either; and such a
+ * caller cannot size and keep a workspace for pkv_decode_attn.
+ *
+ * Same computation and arguments as pkv_decode_attn, without workspace and
+ * workspace_bytes: the scratch is a fixed array of PKV_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library keeps
+ * until the process exits. The function itself allocates nothing.
+ *
+ * - Calls that need more scratch than that (pkv_decode_workspace_size for
+ *   the same batch, num_q_heads, cache and num_parts) return
+ *   PKV_ERR_WORKSPACE and launch nothing.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - All calls share the one array and it keeps the last call's contents;
+ *   nothing in it needs to start at zero, since each call rewrites every part
+ *   it later reads. Calls whose work overlaps on the GPU (other streams, other
+ *   host threads) race on it: order them, e.g. on one stream.
+ * ------------------------------------------------------------------------ */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+pkv_status pkv_decode_attn_noalloc(const void *q, pkv_dtype q_dtype,
+                                   const void *k_cache, const void *v_cache,
+                                   const float *k_scales, const float *v_scales,
+                                   const pkv_cache_desc *cache,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t batch,
+                                   int32_t num_q_heads, float softmax_scale, void *out,
+                                   int32_t num_parts, uint32_t *dev_status,
+                                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

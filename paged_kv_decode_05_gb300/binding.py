@@ -51,6 +51,8 @@ _SIGS = {
     "pkv_decode_split": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
                                         _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_decode_combine": (ctypes.c_int, [_DESC, _I32, _I32, ctypes.c_int, _P, _P, _SZ, _I32, _P]),
+    "pkv_decode_attn_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32,
+                                               _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P]),
 }
 
 
@@ -178,3 +180,22 @@ def pkv_decode_combine(out, k_cache, workspace, num_parts=0, stream=None):
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     int(num_parts), _stream(stream))
     _check("pkv_decode_combine", code)
+
+
+def pkv_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, out,
+                            k_scales=None, v_scales=None, num_parts=0, dev_status=None,
+                            stream=None):
+    """:func:`pkv_decode_attn` using the library's built-in scratch array.
+
+    For callers that cannot allocate device memory: no workspace is passed and
+    nothing is allocated. Raises PkvError(PKV_ERR_WORKSPACE) when the sizes
+    need more scratch than the built-in array holds.
+    """
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    code = lib().pkv_decode_attn_noalloc(
+        _ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        B, Hq, float(softmax_scale), _ptr(out), int(num_parts), _ptr(dev_status),
+        _stream(stream))
+    _check("pkv_decode_attn_noalloc", code)

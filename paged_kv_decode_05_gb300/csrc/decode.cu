@@ -818,3 +818,67 @@ extern "C" pkv_status pkv_decode_combine(const pkv_cache_desc* cache, int32_t ba
                       nullptr, 0, nullptr, batch, num_q_heads, 1.0f, out,
                       const_cast<void*>(workspace), workspace_bytes, num_parts, nullptr, stream);
 }
+
+// ------------------------------------------------ no-allocation variant ---
+// pkv_decode_attn_noalloc: the same split + combine, with the scratch taken
+// from a fixed array compiled into this file instead of a caller workspace.
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+// Device-resident scratch. In host code this name is only a stand-in; the
+// device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Once per device, with that device current: resolve the array's address.
+pkv_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return PKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_decode_attn_noalloc(const void* q, pkv_dtype q_dtype,
+                                              const void* k_cache, const void* v_cache,
+                                              const float* k_scales, const float* v_scales,
+                                              const pkv_cache_desc* cache,
+                                              const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, int32_t batch,
+                                              int32_t num_q_heads, float softmax_scale,
+                                              void* out, int32_t num_parts,
+                                              uint32_t* dev_status, cudaStream_t stream) {
+    Ops ops;
+    int G = 0;
+    pkv_status s = check_decode(cache, batch, num_q_heads, q_dtype, &ops, &G);
+    if (s != PKV_OK) return s;
+    if (batch == 0) return PKV_OK;
+    if (num_parts < 0) return PKV_ERR_INVALID_ARG;
+    const long long workers = num_parts > 0 ? num_parts : default_workers(ops, batch);
+    if (workers <= 0 || workers > 0x7fffffffLL) return workers <= 0 ? PKV_ERR_CUDA : PKV_ERR_INVALID_ARG;
+    if (layout(batch, cache->num_kv_heads, G, cache->head_dim, workers).total > kNoAllocScratchBytes)
+        return PKV_ERR_WORKSPACE;  // needs more scratch than the built-in array holds
+    void* ws = nullptr;
+    s = noalloc_scratch(&ws);
+    if (s != PKV_OK) return s;
+    return run_decode(true, true, q, q_dtype, k_cache, v_cache, k_scales, v_scales, cache,
+                      block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                      softmax_scale, out, ws, kNoAllocScratchBytes, int32_t(workers), dev_status,
+                      stream);
+}
