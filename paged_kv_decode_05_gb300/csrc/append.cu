@@ -27,6 +27,8 @@ __global__ void append_copy_kernel(const uint4* __restrict__ k_new, const uint4*
                                    const int64_t* __restrict__ slots, uint4* __restrict__ k_cache,
                                    uint4* __restrict__ v_cache, int n_tokens, int hkv,
                                    int vec_per_row, long long pool_slots, uint32_t* status) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long long per_tok = (long long)hkv * vec_per_row;
     const long long total = (long long)n_tokens * per_tok;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -97,6 +99,8 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 __global__ void i8_clear_kernel(I8Args a) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long long items = (long long)a.n_tokens * a.hkv;
     for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
          it += ((long long)gridDim.x * blockDim.x) >> 5) {
@@ -112,6 +116,8 @@ __global__ void i8_clear_kernel(I8Args a) {
 
 template <typename S, int D>
 __global__ void i8_absmax_kernel(I8Args a) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long long items = (long long)a.n_tokens * a.hkv;
     for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
          it += ((long long)gridDim.x * blockDim.x) >> 5) {
@@ -177,6 +183,8 @@ __device__ __forceinline__ void settle_tile(int8_t* cache, float* scales, uint32
 
 template <int D>
 __global__ void i8_scale_kernel(I8Args a) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long long items = (long long)a.n_tokens * a.hkv;
     for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
          it += ((long long)gridDim.x * blockDim.x) >> 5) {
@@ -191,6 +199,8 @@ __global__ void i8_scale_kernel(I8Args a) {
 
 template <typename S, int D>
 __global__ void i8_quant_kernel(I8Args a) {
+    griddep_wait();
+    griddep_launch_dependents();
     constexpr int EPL = D / 32;
     const long long items = (long long)a.n_tokens * a.hkv;
     const int lane = threadIdx.x & 31;
@@ -239,10 +249,10 @@ template <typename S, int D>
 void launch_i8(const I8Args& a, cudaStream_t st) {
     const long long items = (long long)a.n_tokens * a.hkv;
     const int g = grid_for(items, kWarps, 1 << 16);
-    i8_clear_kernel<<<g, kThreads, 0, st>>>(a);
-    i8_absmax_kernel<S, D><<<g, kThreads, 0, st>>>(a);
-    i8_scale_kernel<D><<<g, kThreads, 0, st>>>(a);
-    i8_quant_kernel<S, D><<<g, kThreads, 0, st>>>(a);
+    launch_pdl(i8_clear_kernel, dim3(g), dim3(kThreads), 0, st, a);
+    launch_pdl(i8_absmax_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
+    launch_pdl(i8_scale_kernel<D>, dim3(g), dim3(kThreads), 0, st, a);
+    launch_pdl(i8_quant_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
 }
 
 }  // namespace
@@ -279,10 +289,10 @@ extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, pkv_dtype
         if (src_dtype != cache->kv_dtype) return PKV_ERR_INVALID_ARG;
         const int vpr = D * 2 / 16;
         const long long total = (long long)num_tokens * hkv * vpr;
-        append_copy_kernel<<<grid_for(total, kThreads, 152 * 32), kThreads, 0, stream>>>(
-            static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
-            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, hkv, vpr,
-            pool_slots, dev_status);
+        launch_pdl(append_copy_kernel, dim3(grid_for(total, kThreads, 152 * 32)), dim3(kThreads),
+                   0, stream, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                   slot_mapping, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                   num_tokens, hkv, vpr, pool_slots, dev_status);
     } else {
         if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
         if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))

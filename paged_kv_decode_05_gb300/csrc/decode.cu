@@ -51,7 +51,10 @@ struct Cfg {
     static constexpr int TILE = kBlockSize * D * esize;          // bytes of one K (or V) tile
     static constexpr int ROW = D * esize;                         // bytes of one token row
     static constexpr int STAGE = 2 * TILE;
-    static constexpr int NS = (16384 / STAGE) < 2 ? 2 : (16384 / STAGE);  // stages per warp
+    // Stages per warp: as many as fit ~19 KB per warp with their q slots, so
+    // that 3 CTAs of 4 warps share an SM (at least 2 stages).
+    static constexpr int QBYTES = G * D * 2;   // q rows of one (sequence, kv head)
+    static constexpr int NS = (19456 / (STAGE + QBYTES)) < 2 ? 2 : (19456 / (STAGE + QBYTES));
     // QK mapping: 8 lanes per token row, 4 rows per pass, 4 passes.
     static constexpr int E = D / 8;                               // elements per lane per row
     static constexpr int VB = (E * esize) < 16 ? (E * esize) : 16;  // bytes per vector load
@@ -63,12 +66,15 @@ struct Cfg {
     static constexpr int NVAL = 4 * G;
     static constexpr int NF = NVAL >= 8 ? NVAL / 8 : 1;          // scores per lane afterwards
     // Per-warp shared-memory region.
-    static constexpr int OFF_BAR = NS * STAGE;
-    static constexpr int OFF_META = OFF_BAR + NS * 8;
-    static constexpr int OFF_SCL = OFF_META + NS * 16;
-    static constexpr int OFF_P = OFF_SCL + NS * 8;
-    static constexpr int WARP_BYTES = align_up(OFF_P + kBlockSize * G * 4, 128);
-    static_assert(NS > 0 && (NS & (NS - 1)) == 0, "stage count must be a power of two");
+    static constexpr int OFF_BAR = NS * STAGE;                       // 8-byte mbarriers
+    static constexpr int OFF_META = align_up(OFF_BAR + NS * 8, 16);   // int4 per stage
+    static constexpr int OFF_SCL = OFF_META + NS * 16;                // float2 per stage
+    static constexpr int OFF_P = align_up(OFF_SCL + NS * 8, 16);      // float4 reads
+    // q rows of a piece's (sequence, kv head), copied with its first unit
+    static constexpr int OFF_Q = align_up(OFF_P + kBlockSize * G * 4, 128);
+    static constexpr int WARP_BYTES = align_up(OFF_Q + NS * QBYTES, 128);
+    static_assert(NS >= 2 && NS <= 32, "stage count (one parity bit per stage)");
+    static_assert(STAGE % 128 == 0 && OFF_Q % 128 == 0 && QBYTES % 16 == 0, "copy alignment");
     static_assert(E % EV == 0 && EV % 2 == 0, "lane element layout");
     static_assert(G == 1 || G == 2 || G == 4, "group size");
 };
@@ -76,6 +82,15 @@ struct Cfg {
 // Dynamic shared memory starts with 4 ints of scan scratch, then the block
 // prefix [batch + 1]; the per-warp regions follow, 128-byte aligned.
 __host__ __device__ inline int prefix_bytes(int batch) { return align_up(16 + 4 * (batch + 1), 128); }
+
+// Workers that get units: at most one per kMinUnits units, so every range is
+// non-empty and short batches are not cut into single-block pieces. The split
+// and combine kernels derive it from the same U and agree on it.
+constexpr long long kMinUnits = 4;
+__host__ __device__ inline long long eff_workers(long long U, long long W) {
+    const long long cap = U / kMinUnits;
+    return cap < 1 ? 1 : (cap < W ? cap : W);
+}
 
 struct DecodeParams {
     const void* q;
@@ -168,14 +183,13 @@ __device__ __forceinline__ void xstep(float* v, int bit, int lane, int& base) {
 }
 
 // Load NPAIR pairs of 16-bit values starting at element `off` (16-byte
-// aligned) as float2, times `scale`.
+// aligned) of a shared-memory row block as float2, times `scale`.
 template <typename QT, int NPAIR>
-__device__ __forceinline__ void load_q_pairs(const void* q, long long off, float scale,
-                                             float2* dst) {
+__device__ __forceinline__ void load_q_pairs(const void* q, int off, float scale, float2* dst) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + off);
 #pragma unroll
     for (int v = 0; v < NPAIR / 4; ++v) {
-        const uint4 x = __ldg(src + v);
+        const uint4 x = src[v];
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -238,14 +252,16 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     using C = Cfg<KV, D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
     int* prefix = reinterpret_cast<int*>(smem) + 4;
+    griddep_wait();                 // inputs may come from the previous grid
+    griddep_launch_dependents();    // the combine may start launching
     build_prefix(p, reinterpret_cast<int*>(smem), prefix);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long w = (long long)blockIdx.x * kWarpsPerCta + warp;
-    if (w >= p.workers) return;
     const long long U = (long long)prefix[p.batch] * p.hkv;
-    const long long u0 = w * U / p.workers, u1 = (w + 1) * U / p.workers;
-    if (u0 >= u1) return;
+    const long long W = eff_workers(U, p.workers);
+    if (w >= W || U == 0) return;
+    const long long u0 = w * U / W, u1 = (w + 1) * U / W;
 
     unsigned char* region = smem + prefix_bytes(p.batch) + warp * C::WARP_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(region + C::OFF_BAR);
@@ -260,40 +276,49 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     __syncwarp();
 
     // ---- producer: block-table entries for 32 units at a time, one per lane
-    auto fetch = [&](long long base, int& b, int& kvh, int& j, int& blk) {
+    auto fetch = [&](long long base, int& b, int& kvh, int& j, int& blk, int& len) {
         const long long u = base + lane;
         if (u < u1) {
             decode_unit(u, prefix, p.batch, p.hkv, b, kvh, j);
             blk = __ldg(p.block_tables + (long long)b * p.mb + j);
+            len = clamp_len(__ldg(p.context_lens + b), p.mb, p.status, false);
         } else {
-            b = 0; kvh = 0; j = 0; blk = -1;
+            b = 0; kvh = 0; j = 0; blk = -1; len = 0;
         }
     };
     long long cbase = u0;
-    int cb, ckvh, cj, cblk, xb, xkvh, xj, xblk;
-    fetch(cbase, cb, ckvh, cj, cblk);
-    fetch(cbase + 32, xb, xkvh, xj, xblk);
+    int cb, ckvh, cj, cblk, clen, xb, xkvh, xj, xblk, xlen;
+    fetch(cbase, cb, ckvh, cj, cblk, clen);
+    fetch(cbase + 32, xb, xkvh, xj, xblk, xlen);
 
     auto issue = [&](long long u, int s) {
         int idx = int(u - cbase);
         if (idx >= 32) {
             cbase += 32;
-            cb = xb; ckvh = xkvh; cj = xj; cblk = xblk;
-            fetch(cbase + 32, xb, xkvh, xj, xblk);
+            cb = xb; ckvh = xkvh; cj = xj; cblk = xblk; clen = xlen;
+            fetch(cbase + 32, xb, xkvh, xj, xblk, xlen);
             idx -= 32;
         }
         const int b = __shfl_sync(kFull, cb, idx);
         const int kvh = __shfl_sync(kFull, ckvh, idx);
         const int j = __shfl_sync(kFull, cj, idx);
         const int blk = __shfl_sync(kFull, cblk, idx);
+        const int len = __shfl_sync(kFull, clen, idx);
         if (lane == 0) {
             const uint32_t bar = smem_addr(&bars[s]);
             const bool ok = unsigned(blk) < unsigned(p.num_blocks);
-            meta[s] = make_int4(b, kvh, j, ok ? 1 : 0);
+            const bool first = (u == u0) || (j == 0);   // first unit of a piece
+            meta[s] = make_int4(b, kvh | ((ok ? 1 : 0) << 16) | ((first ? 1 : 0) << 17), j, len);
+            const uint32_t tx = (ok ? 2 * C::TILE : 0) + (first ? C::QBYTES : 0);
+            if (tx) mbar_arrive_expect_tx(bar, tx);
+            else mbar_arrive(bar);
+            if (first)
+                bulk_g2s(smem_addr(region + C::OFF_Q + s * C::QBYTES),
+                         static_cast<const uint16_t*>(p.q) + ((long long)b * p.hq + kvh * G) * D,
+                         C::QBYTES, bar);
             if (ok) {
                 const long long tile = (long long)blk * p.hkv + kvh;
                 unsigned char* st = region + s * C::STAGE;
-                mbar_arrive_expect_tx(bar, 2 * C::TILE);
                 bulk_g2s(smem_addr(st), static_cast<const char*>(p.k_cache) + tile * C::TILE,
                          C::TILE, bar);
                 bulk_g2s(smem_addr(st + C::TILE),
@@ -305,7 +330,6 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                 }
             } else {
                 flag_status(p.status, PKV_DEV_BAD_BLOCK);
-                mbar_arrive(bar);
                 if constexpr (C::kI8) mbar_arrive(bar);
             }
         }
@@ -373,8 +397,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     uint32_t parity = 0;
     long long u = u0;
     bool aborted = false;
-    for (; u < u1; ++u) {
-        const int s = int((u - u0) & (C::NS - 1));
+    int s = 0;                       // stage of unit u
+    for (; u < u1; ++u, s = (s + 1 == C::NS) ? 0 : s + 1) {
         const uint32_t bar = smem_addr(&bars[s]);
         const bool got = mbar_wait_bounded(bar, (parity >> s) & 1u, kWaitLimitNs);
         if (!__all_sync(kFull, got)) {
@@ -384,18 +408,19 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
         }
         parity ^= 1u << s;
         const int4 mt = meta[s];
-        if (mt.x != pb || mt.y != pkvh) {
+        const int flags = mt.y >> 16;
+        if (flags & 2) {  // first unit of a new piece: its q rows came with it
             if (pb >= 0) finalize();
             pb = mt.x;
-            pkvh = mt.y;
+            pkvh = mt.y & 0xffff;
             first_j = mt.z;
-            plen = clamp_len(__ldg(p.context_lens + pb), p.mb, p.status, false);
-            const long long qoff = ((long long)pb * p.hq + pkvh * G) * D;
+            plen = mt.w;
+            const unsigned char* qs = region + C::OFF_Q + s * C::QBYTES;
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
                 for (int c = 0; c < C::NV; ++c)
-                    load_q_pairs<QT, C::EV / 2>(p.q, qoff + h * D + c * 8 * C::EV + r8 * C::EV,
+                    load_q_pairs<QT, C::EV / 2>(qs, h * D + c * 8 * C::EV + r8 * C::EV,
                                                 p.qscale, &q2[h][c * C::EV / 2]);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -408,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
         }
         last_j = mt.z;
 
-        if (mt.w) {
+        if (flags & 1) {
             const unsigned char* kt = region + s * C::STAGE;
             const unsigned char* vt = kt + C::TILE;
             const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
@@ -517,9 +542,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     }
     // A copy never completed: give the others a short bounded wait, then leave.
     for (long long v = u; v < u_issue; ++v) {
-        const int s = int((v - u0) & (C::NS - 1));
-        mbar_wait_bounded(smem_addr(&bars[s]), (parity >> s) & 1u, kDrainLimitNs);
-        parity ^= 1u << s;
+        const int sv = int((v - u0) % C::NS);
+        mbar_wait_bounded(smem_addr(&bars[sv]), (parity >> sv) & 1u, kDrainLimitNs);
+        parity ^= 1u << sv;
     }
 }
 
@@ -537,54 +562,82 @@ __device__ __forceinline__ long long worker_of(long long u, long long U, long lo
     return ((u + 1) * W - 1) / U;
 }
 
-// With fewer units than workers some ranges are empty; they write nothing.
-__device__ __forceinline__ bool worker_nonempty(long long w, long long U, long long W) {
-    return w * U / W < (w + 1) * U / W;
+constexpr int kCombineThreads = 256;
+
+// Fold one partial state (m, l, o) into a running merge (M, den, num), all in
+// base 2: the running sums are rescaled when the maximum grows.
+__device__ __forceinline__ void merge_state(float& M, float& den, float4& num, float m, float l,
+                                            const float4& o) {
+    if (m == -INFINITY) return;              // piece saw no valid token
+    if (m > M) {
+        const float r = (M == -INFINITY) ? 0.f : fast_exp2(M - m);
+        den *= r;
+        num.x *= r; num.y *= r; num.z *= r; num.w *= r;
+        M = m;
+    }
+    const float a = fast_exp2(m - M);
+    den += a * l;
+    num.x += a * o.x; num.y += a * o.y; num.z += a * o.z; num.w += a * o.w;
 }
 
 // One CTA per segment (sequence b, kv head): merge the pieces' states
 // out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i (scores are in log2
 // units), or write zeros for an empty sequence. Segments finished inside one
-// worker were written by the split kernel and are skipped.
+// worker were written by the split kernel and are skipped. The CTA's threads
+// form GROUPS groups of G*D/4 threads (one float4 of output each); group k
+// merges pieces k, k + GROUPS, ... and the groups are merged in shared memory.
 template <typename QT, int D, int G>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const CombineParams c) {
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const CombineParams c) {
+    constexpr int Q = D / 4, ITEMS = G * Q, GROUPS = kCombineThreads / ITEMS;
+    static_assert(kCombineThreads % ITEMS == 0, "item layout");
+    __shared__ float s_m[kCombineThreads], s_den[kCombineThreads];
+    __shared__ float4 s_num[kCombineThreads];
+    griddep_wait();                 // partials come from the split grid
+    griddep_launch_dependents();
     const int seg = blockIdx.x;
     const int b = seg / c.hkv, kvh = seg - b * c.hkv;
     const int* P = c.ws_prefix;
     const int nb = P[b + 1] - P[b];
-    constexpr int Q = D / 4;
-    const long long obase = ((long long)b * c.hq + kvh * G) * D;
+    const int t = threadIdx.x, item = t % ITEMS, grp = t / ITEMS;
+    const int h = item / Q, d4 = item - h * Q;
+    const long long obase = ((long long)b * c.hq + kvh * G + h) * D + d4 * 4;
     if (nb == 0) {
-        for (int it = threadIdx.x; it < G * Q; it += blockDim.x) {
+        if (grp == 0) {
             const float2 z[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            store_out<QT, 4>(c.out, obase + (long long)it * 4, z, 0.f);
+            store_out<QT, 4>(c.out, obase, z, 0.f);
         }
         return;
     }
     const long long U = (long long)P[c.batch] * c.hkv;
+    const long long W = eff_workers(U, c.workers);
     const long long uf = (long long)c.hkv * P[b] + (long long)kvh * nb;
-    const long long wf = worker_of(uf, U, c.workers), wl = worker_of(uf + nb - 1, U, c.workers);
+    const long long wf = worker_of(uf, U, W), wl = worker_of(uf + nb - 1, U, W);
     if (wf == wl) return;
-    for (int it = threadIdx.x; it < G * Q; it += blockDim.x) {
-        const int h = it / Q, d4 = it - h * Q;
-        float M = -INFINITY;
-        for (long long w = wf; w <= wl; ++w)
-            if (worker_nonempty(w, U, c.workers)) M = fmaxf(M, c.part_ml[((seg + w) * G + h) * 2]);
-        float den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (long long w = wf; w <= wl; ++w) {
-            if (!worker_nonempty(w, U, c.workers)) continue;  // wrote no piece
-            const long long slot = seg + w;
-            const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + (slot * G + h) * 2);
-            const float a = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-            const float4 o = *reinterpret_cast<const float4*>(c.part_o + (slot * G + h) * D + d4 * 4);
-            den += a * ml.y;
-            num.x += a * o.x; num.y += a * o.y; num.z += a * o.z; num.w += a * o.w;
-        }
-        const float inv = den > 0.f ? 1.0f / den : 0.f;
-        const float2 v[2] = {make_float2(num.x, num.y), make_float2(num.z, num.w)};
-        store_out<QT, 4>(c.out, obase + (long long)h * D + d4 * 4, v, inv);
+    float M = -INFINITY, den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (long long w = wf + grp; w <= wl; w += GROUPS) {
+        const long long slot = seg + w;
+        const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + (slot * G + h) * 2);
+        const float4 o = *reinterpret_cast<const float4*>(c.part_o + (slot * G + h) * D + d4 * 4);
+        merge_state(M, den, num, ml.x, ml.y, o);
     }
+    if constexpr (GROUPS > 1) {
+        s_m[t] = M;
+        s_den[t] = den;
+        s_num[t] = num;
+        __syncthreads();
+        if (grp != 0) return;
+#pragma unroll
+        for (int k = 1; k < GROUPS; ++k) {
+            const int o = k * ITEMS + item;
+            // s_num holds unnormalised sums relative to s_m: merge as a state
+            merge_state(M, den, num, s_m[o], s_den[o], s_num[o]);
+        }
+    }
+    const float inv = den > 0.f ? 1.0f / den : 0.f;
+    const float2 v[2] = {make_float2(num.x, num.y), make_float2(num.z, num.w)};
+    store_out<QT, 4>(c.out, obase, v, inv);
 }
 
 // ------------------------------------------------------------------- host ---
@@ -609,10 +662,10 @@ struct Impl {
             blocks, decode_split_kernel<KV, QT, D, G>, kThreads, smem);
     }
     static void split(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-        decode_split_kernel<KV, QT, D, G><<<grid, kThreads, smem, st>>>(p);
+        launch_pdl(decode_split_kernel<KV, QT, D, G>, dim3(grid), dim3(kThreads), smem, st, p);
     }
     static void combine(const CombineParams& c, int grid, cudaStream_t st) {
-        decode_combine_kernel<QT, D, G><<<grid, 128, 0, st>>>(c);
+        launch_pdl(decode_combine_kernel<QT, D, G>, dim3(grid), dim3(kCombineThreads), 0, st, c);
     }
     static Ops ops() { return Ops{Cfg<KV, D, G>::WARP_BYTES, prepare, occupancy, split, combine}; }
 };
@@ -669,7 +722,8 @@ pkv_status check_decode(const pkv_cache_desc* c, int batch, int hq, pkv_dtype q_
         return PKV_ERR_INVALID_ARG;
     if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
     if (batch < 0 || hq <= 0 || hq % c->num_kv_heads) return PKV_ERR_INVALID_ARG;
-    if (c->block_size != kBlockSize || batch > kMaxBatch) return PKV_ERR_UNSUPPORTED;
+    if (c->block_size != kBlockSize || batch > kMaxBatch || c->num_kv_heads > 0xffff)
+        return PKV_ERR_UNSUPPORTED;
     if (c->kv_dtype != PKV_I8 && q_dtype != c->kv_dtype) return PKV_ERR_INVALID_ARG;
     *G = hq / c->num_kv_heads;
     if (!pick_ops(c->kv_dtype, q_dtype, c->head_dim, *G, ops)) return PKV_ERR_UNSUPPORTED;
