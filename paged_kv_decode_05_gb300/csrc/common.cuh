@@ -35,15 +35,25 @@ __device__ __forceinline__ float2 unpack2(F16, uint32_t w) {
     __half2 h = *reinterpret_cast<__half2*>(&w);
     return __half22float2(h);
 }
-// Four packed int8 codes -> four floats, exact. Each biased byte (x + 128)
-// becomes the low mantissa byte of 2^23, so the float is 2^23 + 128 + x.
-__device__ __forceinline__ void unpack4_i8(uint32_t w, float* f) {
-    const uint32_t u = w ^ 0x80808080u;
-    const float bias = 8388736.0f;  // 2^23 + 128
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - bias;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - bias;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - bias;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - bias;
+// Two int8 codes (selected bytes of a word already XOR-ed with 0x80808080,
+// i.e. biased to x + 128) -> fp16x2 holding the codes exactly: the byte
+// becomes the low mantissa byte of 1024 (fp16 0x6400), then 1152 is
+// subtracted. `sel` picks the bytes: 0x4140 -> bytes 0,1; 0x4342 -> bytes 2,3.
+__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t biased, uint32_t sel) {
+    const uint32_t h = __byte_perm(biased, 0x64646464u, sel);
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// d += a * b on the tensor cores: m16n8k16, fp16 inputs, fp32 accumulators
+// (a: 4 registers of the row-major 16x16 tile, b: 2 of the 16x8 tile).
+__device__ __forceinline__ void mma_16816_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float load_scalar(BF16, const void* p, long i) {

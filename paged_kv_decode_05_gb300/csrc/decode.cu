@@ -75,7 +75,7 @@ struct Cfg {
     static constexpr int WARP_BYTES = align_up(OFF_Q + NS * QBYTES, 128);
     static_assert(NS >= 2 && NS <= 32, "stage count (one parity bit per stage)");
     static_assert(STAGE % 128 == 0 && OFF_Q % 128 == 0 && QBYTES % 16 == 0, "copy alignment");
-    static_assert(E % EV == 0 && EV % 2 == 0, "lane element layout");
+    static_assert(E % EV == 0 && EV % 2 == 0 && NV >= 1, "lane element layout");
     static_assert(G == 1 || G == 2 || G == 4, "group size");
 };
 
@@ -218,13 +218,21 @@ __device__ __forceinline__ void load_pairs_smem(const unsigned char* src, float2
 #pragma unroll
         for (int i = 0; i < VB / 4; ++i) dst[i] = unpack2(KV{}, w[i]);
     } else {
+        // int8 codes -> floats: biased byte as the low mantissa byte of 2^23,
+        // then one packed subtraction of 2^23 + 128 per pair (exact)
         constexpr int NW = VB >= 4 ? VB / 4 : 1;
+        const float2 bias = make_float2(-8388736.0f, -8388736.0f);
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
-            float f[4];
-            unpack4_i8(w[i], f);
-            dst[2 * i] = make_float2(f[0], f[1]);
-            if (VB >= 4) dst[2 * i + 1] = make_float2(f[2], f[3]);
+            const uint32_t u = w[i] ^ 0x80808080u;
+            dst[2 * i] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                                                __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
+                                    bias);
+            if (VB >= 4)
+                dst[2 * i + 1] = __fadd2_rn(
+                    make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                                __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
+                    bias);
         }
     }
 }
@@ -351,16 +359,30 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
     const int h0 = xbase % G;                     // first head of the lane's scores
     const bool dup = (G == 1) && (lane & 1);      // G == 1: lane pairs hold one score
 
-    float2 q2[G][C::E / 2];
-    float m[G], lsum[C::NF];
+    // INT8 caches compute scores on the tensor cores (mma.sync m16n8k16, K
+    // codes exact in fp16, fp32 accumulators): rows = the tile's 16 tokens,
+    // columns = the g heads (padded to 8). Lane (gq, tq) = (lane / 4, lane % 4)
+    // then holds tokens gq and gq + 8 of heads 2tq and 2tq + 1.
+    constexpr bool kMma = C::kI8;
+    constexpr int LS = kMma ? 2 : C::NF;         // lane partial sums of l
+    const int gq = lane >> 2, tq = lane & 3;
+    float2 q2[kMma ? 1 : G][kMma ? 1 : C::E / 2];
+    uint32_t qb[kMma ? D / 16 : 1][2];           // fp16x2 B fragments of q
+    float m[G], lsum[LS];
     float2 o2[G][C::DPL / 2];
     int pb = -1, pkvh = -1, first_j = 0, last_j = 0, plen = 0;
+
+    // Does this lane's lsum hold a partial of head hh, and at which index?
+    auto owns = [&](int hh) -> bool {
+        if constexpr (kMma) return (hh >> 1) == tq;
+        else return hh / C::NF == h0 / C::NF && !dup;
+    };
+    auto lidx = [&](int hh) -> int { return kMma ? (hh & 1) : hh % C::NF; };
 
     auto finalize = [&]() {
         float lh[G];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-            lh[hh] = (hh / C::NF == h0 / C::NF && !dup) ? lsum[hh % C::NF] : 0.f;
+        for (int hh = 0; hh < G; ++hh) lh[hh] = owns(hh) ? lsum[lidx(hh)] : 0.f;
 #pragma unroll
         for (int off = 16; off; off >>= 1)
 #pragma unroll
@@ -416,12 +438,31 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
             first_j = mt.z;
             plen = mt.w;
             const unsigned char* qs = region + C::OFF_Q + s * C::QBYTES;
+            if constexpr (kMma) {
+                // lane's dims for k-step kk: 16*tq + 4*(kk%4) + 64*(kk/4) + {0..3}
+                // (a fixed permutation of the contraction index, shared with K)
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    qb[kk][0] = qb[kk][1] = 0u;
+                    if (gq < G) {
+                        const int d0 = 16 * tq + 4 * (kk % 4) + 64 * (kk / 4);
+                        const uint2 x = *reinterpret_cast<const uint2*>(
+                            qs + 2 * (gq * D + d0));
+                        const float2 f0 = unpack2(QT{}, x.x), f1 = unpack2(QT{}, x.y);
+                        const __half2 h0v = __floats2half2_rn(f0.x, f0.y);
+                        const __half2 h1v = __floats2half2_rn(f1.x, f1.y);
+                        qb[kk][0] = *reinterpret_cast<const uint32_t*>(&h0v);
+                        qb[kk][1] = *reinterpret_cast<const uint32_t*>(&h1v);
+                    }
+                }
+            } else {
 #pragma unroll
-                for (int c = 0; c < C::NV; ++c)
-                    load_q_pairs<QT, C::EV / 2>(qs, h * D + c * 8 * C::EV + r8 * C::EV,
-                                                p.qscale, &q2[h][c * C::EV / 2]);
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int c = 0; c < C::NV; ++c)
+                        load_q_pairs<QT, C::EV / 2>(qs, h * D + c * 8 * C::EV + r8 * C::EV,
+                                                    p.qscale, &q2[h][c * C::EV / 2]);
+            }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 m[h] = -INFINITY;
@@ -429,7 +470,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                 for (int i = 0; i < C::DPL / 2; ++i) o2[h][i] = make_float2(0.f, 0.f);
             }
 #pragma unroll
-            for (int x = 0; x < C::NF; ++x) lsum[x] = 0.f;
+            for (int x = 0; x < LS; ++x) lsum[x] = 0.f;
         }
         last_j = mt.z;
 
@@ -443,61 +484,119 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                 ksc = sc.x;
                 vsc = sc.y;
             }
-            // scores: acc[k*G + h] = <q_h, K[rgrp + 4k]> over the lane's dims
-            float acc[C::NVAL];
+            float alpha[G];
+            if constexpr (kMma) {
+                // scores on the tensor cores: rows gq, gq + 8 of the tile, the
+                // lane's 16-byte chunk of each half row holds 4 k-steps' columns
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                uint32_t w0[D / 16], w1[D / 16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const unsigned char* row = kt + (rgrp + 4 * k) * C::ROW;
-                float2 kf[C::E / 2];
-#pragma unroll
-                for (int c = 0; c < C::NV; ++c)
-                    load_pairs_smem<KV, C::VB>(row + c * 8 * C::VB + r8 * C::VB,
-                                               &kf[c * C::EV / 2]);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int i = 0; i < C::E / 2; ++i) a = __ffma2_rn(q2[h][i], kf[i], a);
-                    acc[k * G + h] = a.x + a.y;
+                for (int c = 0; c < D / 64; ++c) {
+                    const uint4 x0 = *reinterpret_cast<const uint4*>(kt + gq * C::ROW + 64 * c + 16 * tq);
+                    const uint4 x1 = *reinterpret_cast<const uint4*>(kt + (gq + 8) * C::ROW + 64 * c + 16 * tq);
+                    w0[4 * c] = x0.x; w0[4 * c + 1] = x0.y; w0[4 * c + 2] = x0.z; w0[4 * c + 3] = x0.w;
+                    w1[4 * c] = x1.x; w1[4 * c + 1] = x1.y; w1[4 * c + 2] = x1.z; w1[4 * c + 3] = x1.w;
                 }
-            }
-            int xb = 0;
-            xstep<C::NVAL>(acc, 4, lane, xb);
-            xstep<(C::NVAL >= 2 ? C::NVAL / 2 : 1)>(acc, 2, lane, xb);
-            xstep<(C::NVAL >= 4 ? C::NVAL / 4 : 1)>(acc, 1, lane, xb);
-            float sc[C::NF];
 #pragma unroll
-            for (int x = 0; x < C::NF; ++x) sc[x] = (my_t < nv) ? acc[x] * ksc : -INFINITY;
-            // per-head block max, new running max, rescale factors
-            float bm[G];
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t u0 = w0[kk] ^ 0x80808080u, u1 = w1[kk] ^ 0x80808080u;
+                    mma_16816_f16(acc[kk & 1], i8x2_to_h2(u0, 0x4140), i8x2_to_h2(u1, 0x4140),
+                                  i8x2_to_h2(u0, 0x4342), i8x2_to_h2(u1, 0x4342),
+                                  qb[kk][0], qb[kk][1]);
+                }
+                const float sk = p.qscale * ksc;
+                float sv[2][2];   // [token gq / gq + 8][head 2tq + e]
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh)
-                bm[hh] = (hh / C::NF == h0 / C::NF) ? sc[hh % C::NF] : -INFINITY;
+                for (int e = 0; e < 2; ++e) {
+                    const bool hv = 2 * tq + e < G;
+                    sv[0][e] = (hv && gq < nv) ? (acc[0][e] + acc[1][e]) * sk : -INFINITY;
+                    sv[1][e] = (hv && gq + 8 < nv) ? (acc[0][2 + e] + acc[1][2 + e]) * sk : -INFINITY;
+                }
+                float bme[2];
 #pragma unroll
-            for (int off = 16; off; off >>= 1)
+                for (int e = 0; e < 2; ++e) {
+                    bme[e] = fmaxf(sv[0][e], sv[1][e]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1)
+                        bme[e] = fmaxf(bme[e], __shfl_xor_sync(kFull, bme[e], off));
+                }
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float bmh = __shfl_sync(kFull, bme[hh & 1], hh >> 1);
+                    const float mn = fmaxf(m[hh], bmh);
+                    alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m[hh] - mn);
+                    m[hh] = mn;
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float mh = m[e < G ? e : 0], ah = alpha[e < G ? e : 0];
+#pragma unroll
+                    for (int cand = 1; cand < (G + 1) / 2; ++cand)
+                        if (tq == cand) { mh = m[2 * cand + e]; ah = alpha[2 * cand + e]; }
+                    const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mh);
+                    const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mh);
+                    lsum[e] = lsum[e] * ah + p0 + p1;
+                    if (2 * tq + e < G) {
+                        pbuf[gq * G + 2 * tq + e] = p0 * vsc;
+                        pbuf[(gq + 8) * G + 2 * tq + e] = p1 * vsc;
+                    }
+                }
+            } else {
+                // scores: acc[k*G + h] = <q_h, K[rgrp + 4k]> over the lane's dims
+                float acc[C::NVAL];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const unsigned char* row = kt + (rgrp + 4 * k) * C::ROW;
+                    float2 kf[C::E / 2];
+#pragma unroll
+                    for (int c = 0; c < C::NV; ++c)
+                        load_pairs_smem<KV, C::VB>(row + c * 8 * C::VB + r8 * C::VB,
+                                                   &kf[c * C::EV / 2]);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int i = 0; i < C::E / 2; ++i) a = __ffma2_rn(q2[h][i], kf[i], a);
+                        acc[k * G + h] = a.x + a.y;
+                    }
+                }
+                int xb = 0;
+                xstep<C::NVAL>(acc, 4, lane, xb);
+                xstep<(C::NVAL >= 2 ? C::NVAL / 2 : 1)>(acc, 2, lane, xb);
+                xstep<(C::NVAL >= 4 ? C::NVAL / 4 : 1)>(acc, 1, lane, xb);
+                float sc[C::NF];
+#pragma unroll
+                for (int x = 0; x < C::NF; ++x) sc[x] = (my_t < nv) ? acc[x] * ksc : -INFINITY;
+                // per-head block max, new running max, rescale factors
+                float bm[G];
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh)
-                    bm[hh] = fmaxf(bm[hh], __shfl_xor_sync(kFull, bm[hh], off));
-            float alpha[G];
+                    bm[hh] = (hh / C::NF == h0 / C::NF) ? sc[hh % C::NF] : -INFINITY;
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float mn = fmaxf(m[hh], bm[hh]);
-                alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m[hh] - mn);
-                m[hh] = mn;
-            }
-            float pr[C::NF];
+                for (int off = 16; off; off >>= 1)
 #pragma unroll
-            for (int x = 0; x < C::NF; ++x) {
-                float mh = m[x], ah = alpha[x];
+                    for (int hh = 0; hh < G; ++hh)
+                        bm[hh] = fmaxf(bm[hh], __shfl_xor_sync(kFull, bm[hh], off));
+    #pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float mn = fmaxf(m[hh], bm[hh]);
+                    alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m[hh] - mn);
+                    m[hh] = mn;
+                }
+                float pr[C::NF];
 #pragma unroll
-                for (int cand = 1; cand < G / C::NF; ++cand)
-                    if (h0 == cand * C::NF) { mh = m[cand * C::NF + x]; ah = alpha[cand * C::NF + x]; }
-                pr[x] = (sc[x] == -INFINITY) ? 0.f : fast_exp2(sc[x] - mh);
-                lsum[x] = lsum[x] * ah + pr[x];
-            }
-            if (!dup) {
+                for (int x = 0; x < C::NF; ++x) {
+                    float mh = m[x], ah = alpha[x];
 #pragma unroll
-                for (int x = 0; x < C::NF; ++x) pbuf[my_t * G + h0 + x] = pr[x] * vsc;
+                    for (int cand = 1; cand < G / C::NF; ++cand)
+                        if (h0 == cand * C::NF) { mh = m[cand * C::NF + x]; ah = alpha[cand * C::NF + x]; }
+                    pr[x] = (sc[x] == -INFINITY) ? 0.f : fast_exp2(sc[x] - mh);
+                    lsum[x] = lsum[x] * ah + pr[x];
+                }
+                if (!dup) {
+#pragma unroll
+                    for (int x = 0; x < C::NF; ++x) pbuf[my_t * G + h0 + x] = pr[x] * vsc;
+                }
             }
 #pragma unroll
             for (int h = 0; h < G; ++h)
