@@ -14,7 +14,7 @@ The oracle is plain and slow on purpose:
 * ``append`` -- the KV-cache write: a bit copy for fp16/bf16 caches and the
   INT8 quantise-on-append rule with per-(block, kv_head) fp32 scales, written
   with NumPy float32 operations so that each IEEE round-to-nearest step is the
-  same one the kernel takes.
+  same one the kernel takes. Also the copy-on-write block copy.
 
 Conventions: ``np.uint16`` arrays hold bfloat16 bit patterns, ``np.float16``
 arrays hold fp16 values, ``np.int8`` arrays hold quantised codes. Caches are
@@ -47,4 +47,5 @@ from .append import (  # noqa: F401
     quantize_int8,
     requantize_int8,
     bf16_bits_to_f32,
+    copy_blocks,
 )

@@ -128,3 +128,27 @@ def append_int8(k_cache, v_cache, k_scales, v_scales, k_new, v_new,
     v_new = np.asarray(v_new, dtype=np.float32)
     _append_int8_one(k_cache, k_scales, k_new, slots, block_size)
     _append_int8_one(v_cache, v_scales, v_new, slots, block_size)
+
+
+def copy_blocks(k_cache, v_cache, src_blocks, dst_blocks, k_scales=None, v_scales=None):
+    """Copy whole physical blocks ``src -> dst`` (all kv heads, K and V, and
+    the INT8 scales when given), pair by pair in order (in place).
+
+    The copy-on-write step of a paged KV cache: a block shared by several
+    sequences (reference count > 1) gets a private copy before one of them
+    writes to it, and speculative decoding rolls a rejected draft back to such
+    copies (Continuous-Batching-LLM-Inference-Engine README, feature list
+    "Paged KV-cache": copy-on-write reference counting; "Speculative
+    decoding": KV-cache rollback uses the copy-on-write). Reading: a pair
+    with an id outside the pool is skipped; a destination that is also a
+    source in the same call is a caller error.
+    """
+    NB = k_cache.shape[0]
+    for s, d in zip(np.asarray(src_blocks).tolist(), np.asarray(dst_blocks).tolist()):
+        if not (0 <= s < NB and 0 <= d < NB):
+            continue
+        k_cache[d] = k_cache[s]
+        v_cache[d] = v_cache[s]
+        if k_scales is not None:
+            k_scales[d] = k_scales[s]
+            v_scales[d] = v_scales[s]

@@ -199,3 +199,26 @@ def test_golden_catches_planted_quantiser_mistakes(mistake):
         if codes[:8].tolist() != call["codes_rows_0_7"] or s != call["scale"]:
             diverged = True
     assert diverged
+
+
+def test_copy_blocks_round_trip_canaries_and_order():
+    from oracle import copy_blocks
+    rng = np.random.default_rng(9)
+    NB, Hkv, D = 12, 2, 8
+    k = rng.integers(0, 1 << 16, size=(NB, Hkv, 16, D)).astype(np.uint16)
+    v = rng.integers(0, 1 << 16, size=(NB, Hkv, 16, D)).astype(np.uint16)
+    ks = rng.random((NB, Hkv)).astype(np.float32)
+    vs = rng.random((NB, Hkv)).astype(np.float32)
+    k0, v0, ks0, vs0 = k.copy(), v.copy(), ks.copy(), vs.copy()
+    src = np.array([3, 5, 0, 99, 7], np.int32)
+    dst = np.array([8, 9, 10, 4, -1], np.int32)    # two pairs out of the pool: skipped
+    copy_blocks(k, v, src, dst, ks, vs)
+    for s_, d_ in ((3, 8), (5, 9), (0, 10)):
+        assert np.array_equal(k[d_], k0[s_]) and np.array_equal(v[d_], v0[s_])
+        assert np.array_equal(ks[d_], ks0[s_]) and np.array_equal(vs[d_], vs0[s_])
+    untouched = [b for b in range(NB) if b not in (8, 9, 10)]
+    assert np.array_equal(k[untouched], k0[untouched]) and np.array_equal(ks[untouched], ks0[untouched])
+    # pairs apply in order: a chain 1 -> 2 -> 6 carries block 1 to block 6
+    k1 = k.copy()
+    copy_blocks(k, v, np.array([1, 2]), np.array([2, 6]))
+    assert np.array_equal(k[6], k1[1]) and np.array_equal(k[2], k1[1])
