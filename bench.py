@@ -47,6 +47,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--config", default="gqa8b", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--op", default="decode_step", choices=["decode_step", "copy_blocks"],
+                    help="decode_step: the hot path (default); copy_blocks: copy-on-write "
+                         "block copy of --copy-pairs random blocks of the workload's pool")
+    ap.add_argument("--copy-pairs", type=int, default=4096)
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the step from a captured CUDA graph instead of eager launches")
     ap.add_argument("--num-parts", type=int, default=0, help="worker warps (0 = device default)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
@@ -310,6 +316,14 @@ def run_native(args):
     for _ in range(W):
         _step(st, cfg, ws, parts)
     torch.cuda.synchronize(device)
+    graph = None
+    if args.graph:  # one captured step, replayed in the timed loop
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            _step(st, cfg, ws, parts)
+        for _ in range(W):
+            graph.replay()
+        torch.cuda.synchronize(device)
 
     # ---- device-timed region: K steps, inputs resident in HBM
     every = args.event_every
@@ -327,7 +341,10 @@ def run_native(args):
     wall0 = time.time()
     t_start.record()
     for i in range(K):
-        _step(st, cfg, ws, parts, step_ev.get(i) if every > 0 else None)
+        if graph is not None:
+            graph.replay()
+        else:
+            _step(st, cfg, ws, parts, step_ev.get(i) if every > 0 else None)
     t_end.record()
     torch.cuda.synchronize(device)
     wall1 = time.time()
@@ -335,9 +352,9 @@ def run_native(args):
     time.sleep(0.2)
     clocks = sampler.stop(wall0, wall1)
     ms_total = reduce_max(t_start.elapsed_time(t_end), world, device)
-    if every <= 0:  # time the kernels in a second pass of K steps
+    if every <= 0 or graph is not None:  # time the kernels in a separate pass of K steps
         for i in range(K):
-            _step(st, cfg, ws, parts, step_ev[i])
+            _step(st, cfg, ws, parts, step_ev.get(i))
         torch.cuda.synchronize(device)
     evs = list(step_ev.values())
     avg = lambda i, j: sum(e[i].elapsed_time(e[j]) for e in evs) / len(evs)  # noqa: E731
@@ -377,7 +394,9 @@ def run_native(args):
                           "combine": round(combine_avg_ms, 6),
                           "timed_launches": len(evs),
                           "how": f"CUDA events around the kernels of every {every}-th timed step"
-                                 if every > 0 else "CUDA events, separate pass of K steps"},
+                                 if every > 0 and graph is None
+                                 else "CUDA events, separate eager pass of K steps"},
+        "launch_mode": "cuda_graph" if graph is not None else "eager",
         "e2e": e2e, "gpu_launches": K * launches_per_step, "clocks": clocks,
         "device_status": status,
     }
@@ -479,10 +498,54 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_copy_blocks(args):
+    """Copy-on-write block copy throughput on the workload's pool (1 GPU)."""
+    import torch
+    from paged_kv_decode_05_gb300 import binding as B
+    from paged_kv_decode_05_gb300.build import build
+    build()
+    device = torch.device("cuda", 0)
+    cfg = CONFIGS[args.config]
+    w = make_workload(cfg)
+    st = _gpu_state(w, device)
+    rng = np.random.default_rng(1)
+    n = min(args.copy_pairs, w.num_blocks // 2)
+    perm = rng.permutation(w.num_blocks).astype(np.int32)
+    src = torch.from_numpy(perm[:n].copy()).to(device)
+    dst = torch.from_numpy(perm[n:2 * n].copy()).to(device)
+    esz = 1 if cfg.kv_dtype == "i8" else 2
+    block_bytes = cfg.num_kv_heads * cfg.block_size * cfg.head_dim * esz
+    moved = 2 * n * 2 * block_bytes + (2 * 2 * n * cfg.num_kv_heads * 4 if esz == 1 else 0)
+    for _ in range(args.warmup):
+        B.pkv_copy_blocks(st["k_cache"], st["v_cache"], src, dst, st["k_scales"], st["v_scales"])
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        B.pkv_copy_blocks(st["k_cache"], st["v_cache"], src, dst, st["k_scales"], st["v_scales"])
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / args.steps
+    peak, src_name = load_peaks()
+    gbs = moved / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "copy-on-write block copy HBM GB/s (read + write)", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 6), "higher_is_better": True, "dtype": cfg.kv_dtype,
+        "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.config], "pairs": n,
+                                        "bytes_per_pair": 2 * block_bytes},
+        "roofline": {"kernel": "copy_blocks_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": peak, "peak_source": src_name, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None},
+        "gpu_launches": args.steps}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "copy_blocks":
+        run_copy_blocks(args)
     else:
         run_native(args)
 

@@ -187,6 +187,28 @@ pkv_status pkv_decode_combine(const pkv_cache_desc *cache, int32_t batch,
                               int32_t num_parts, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Copy-on-write block copy (fork / rollback)
+ *
+ * Copies whole physical blocks src_blocks[i] -> dst_blocks[i] (all kv heads,
+ * K and V, and for INT8 caches the K and V scales), i < num_pairs: the
+ * private copy a copy-on-write block gets before a sequence writes into it,
+ * and the rollback of a rejected speculative draft onto such copies
+ * (Continuous-Batching-LLM-Inference-Engine README, feature list "Paged
+ * KV-cache": copy-on-write reference counting; "Speculative decoding":
+ * KV-cache rollback uses copy-on-write).
+ *
+ * src_blocks, dst_blocks: device int32 [num_pairs]. A pair with an id outside
+ * [0, num_blocks) is skipped and flagged PKV_DEV_BAD_BLOCK; src == dst is a
+ * no-op. A block that is a destination and also a source in the same call
+ * gives an unspecified result (pairs run in parallel). k_scales, v_scales may
+ * be NULL except for INT8 caches. Caches 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, float *k_scales, float *v_scales,
+                           const pkv_cache_desc *cache, const int32_t *src_blocks,
+                           const int32_t *dst_blocks, int32_t num_pairs, uint32_t *dev_status,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Decode attention without any allocation by anyone
  *
  * No counterpart on the source pages: this variant exists for callers that

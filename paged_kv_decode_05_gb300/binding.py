@@ -51,6 +51,7 @@ _SIGS = {
     "pkv_decode_split": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
                                         _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_decode_combine": (ctypes.c_int, [_DESC, _I32, _I32, ctypes.c_int, _P, _P, _SZ, _I32, _P]),
+    "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _DESC, _P, _P, _I32, _P, _P]),
     "pkv_decode_attn_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32,
                                                _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P]),
 }
@@ -180,6 +181,16 @@ def pkv_decode_combine(out, k_cache, workspace, num_parts=0, stream=None):
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     int(num_parts), _stream(stream))
     _check("pkv_decode_combine", code)
+
+
+def pkv_copy_blocks(k_cache, v_cache, src_blocks, dst_blocks, k_scales=None, v_scales=None,
+                    dev_status=None, stream=None):
+    """Copy whole blocks ``src_blocks[i] -> dst_blocks[i]`` (int32 device tensors)."""
+    desc = cache_desc(k_cache)
+    code = lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                                 ctypes.byref(desc), _ptr(src_blocks), _ptr(dst_blocks),
+                                 int(src_blocks.numel()), _ptr(dev_status), _stream(stream))
+    _check("pkv_copy_blocks", code)
 
 
 def pkv_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, out,
