@@ -10,7 +10,8 @@ The oracle is plain and slow on purpose:
 * ``paged_attention`` -- float64 single-query attention that walks each
   sequence's block table token by token (logical position -> physical block,
   row) and evaluates ``softmax(scale * q K^T) V`` with a max-subtracted
-  softmax. It also holds the partial-state merge (the split-K identity).
+  softmax. It also holds the partial-state merge (the split-K identity) and
+  the multi-query (speculative verification / prefill chunk) causal variant.
 * ``append`` -- the KV-cache write: a bit copy for fp16/bf16 caches and the
   INT8 quantise-on-append rule with per-(block, kv_head) fp32 scales, written
   with NumPy float32 operations so that each IEEE round-to-nearest step is the
@@ -38,6 +39,7 @@ against closed forms, invariants, brute force and hand-worked fixtures under
 from .paged_attention import (  # noqa: F401
     decode_kv,
     paged_decode_attention,
+    paged_multiquery_attention,
     partial_state,
     merge_states,
 )

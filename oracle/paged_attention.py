@@ -131,3 +131,49 @@ def merge_states(states):
         num = num + a * np.asarray(o, dtype=np.float64)
         den = den + a * l
     return num / den
+
+
+def paged_multiquery_attention(q, cu_q, k_cache, v_cache, block_tables, context_lens,
+                               softmax_scale, k_scales=None, v_scales=None, block_size=16,
+                               seqs=None):
+    """Several new query tokens per sequence, causal among themselves (float64).
+
+    The target model of speculative decoding scores the draft's K tokens plus
+    one in a single batched pass (Continuous-Batching-LLM-Inference-Engine
+    README, feature list "Speculative decoding"), and a continuous-batching
+    scheduler mixes decode tokens with prefill chunks (mini-inference-engine
+    overview). Both are attention of ``n_b`` new query tokens per sequence
+    over the paged cache, which already holds them. Reading: sequence ``b``
+    owns query rows ``cu_q[b] .. cu_q[b+1]-1`` (``n_b`` of them, in position
+    order), its cache holds ``L_b = context_lens[b]`` tokens including those
+    ``n_b``, and query ``i`` sits at position ``p_i = L_b - n_b + i`` and attends
+    to positions ``0 .. p_i``.
+
+    q [total_q, Hq, D]; cu_q int [B+1]. Returns float64 rows for the selected
+    sequences' queries, concatenated in sequence order.
+    """
+    total_q, Hq, D = q.shape
+    NB, Hkv, bs, Dk = k_cache.shape
+    assert bs == block_size and Dk == D and Hq % Hkv == 0
+    g = Hq // Hkv
+    B = len(cu_q) - 1
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    rows = []
+    for b in seqs:
+        n = int(cu_q[b + 1] - cu_q[b])
+        L = int(context_lens[b])
+        assert 0 <= n <= L or n == 0
+        out = np.zeros((n, Hq, D), dtype=np.float64)
+        if n:
+            K = _gather_sequence(k_cache, k_scales, block_tables, b, L, bs)
+            V = _gather_sequence(v_cache, v_scales, block_tables, b, L, bs)
+            for i in range(n):
+                p = L - n + i
+                qi = decode_kv(q[int(cu_q[b]) + i])
+                for h in range(Hq):
+                    kvh = h // g
+                    s = float(softmax_scale) * (K[:p + 1, kvh, :] @ qi[h])
+                    w = np.exp(s - s.max())
+                    out[i, h] = (w @ V[:p + 1, kvh, :]) / w.sum()
+        rows.append(out)
+    return np.concatenate(rows, axis=0) if rows else np.zeros((0, Hq, D))
