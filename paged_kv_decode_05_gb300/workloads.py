@@ -15,13 +15,14 @@ Recipe (every config):
   config fixes the pool size, it is the blocks in use plus 10 %, rounded up.
   A seeded permutation of the pool hands out blocks in sequence order, so every
   table is scattered over the pool.
-* Each sequence's last token (position ``L - 1``) is the decode step's new
-  token; positions ``0 .. L - 2`` form the bulk "fill" appended beforehand.
+* Each sequence's last ``q_len`` tokens (positions ``L - q_len .. L - 1``;
+  one token for a decode step) are the step's new tokens; positions
+  ``0 .. L - q_len - 1`` form the bulk "fill" appended beforehand.
 * Prefix sharing (skewed mix): sequences are taken 4 at a time in batch order;
   member ``i`` of a group reads the group's shared physical blocks for its
-  first ``min(prefix, 16 * floor((L_i - 1) / 16))`` tokens, so the block that
-  receives its new token is always private (copy-on-write safe). The shared
-  prefix is written once.
+  first ``min(prefix, 16 * floor((L_i - q_len) / 16))`` tokens, so the blocks
+  that receive its new tokens are always private (copy-on-write safe). The
+  shared prefix is written once.
 
 The five configurations are the shapes of a paged-KV serving loop's decode
 step: a tiny fp16 case, an MHA 7B-shape batch, a Llama-3-8B-shape GQA batch
@@ -59,6 +60,7 @@ class DecodeConfig:
     share_group: int = 4
     seed: int = 0
     block_size: int = BLOCK_SIZE
+    q_len: int = 1         # new query tokens per sequence (1 = decode)
 
     @property
     def group(self) -> int:
@@ -96,6 +98,14 @@ CONFIGS = {
         kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
         len_groups=((8, 32768, 131072), (120, 16, 256)), max_len=131072,
         prefix_share=2048),
+    "spec_verify": DecodeConfig(
+        name="spec_verify", batch=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
+        len_groups=((256, 128, 4096),), max_len=4096, q_len=5),
+    "prefill_chunk": DecodeConfig(
+        name="prefill_chunk", batch=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
+        len_groups=((8, 512, 8192),), max_len=8192, q_len=512),
 }
 
 # One-line workload descriptions, for bench output and docs.
@@ -106,6 +116,10 @@ DESCRIPTIONS = {
     "gqa8b_int8": "GQA Llama-3-8B-shape INT8 KV: B=256, 32/8 heads, D=128, L~U[128,4096]",
     "skewed": "skewed long-context bf16: 8 x L~U[32768,131072] + 120 x L~U[16,256], "
               "32/8 heads, D=128, 2048-token CoW prefix per 4 sequences",
+    "spec_verify": "speculative verification bf16: B=256, 4 draft tokens + 1 per sequence, "
+                   "32/8 heads, D=128, L~U[128,4096]",
+    "prefill_chunk": "chunked prefill bf16: B=8, 512-token chunk per sequence after a cached "
+                     "prefix, 32/8 heads, D=128, L~U[512,8192]",
 }
 
 
@@ -160,9 +174,10 @@ class Workload:
     fill_slots: np.ndarray            # int64 [Nf]
     k_fill: np.ndarray                # [Nf, Hkv, D] source dtype
     v_fill: np.ndarray
-    step_slots: np.ndarray            # int64 [B], -1 if L == 0
-    k_step: np.ndarray                # [B, Hkv, D] source dtype
+    step_slots: np.ndarray            # int64 [B*q_len], -1 if L == 0
+    k_step: np.ndarray                # [B*q_len, Hkv, D] source dtype
     v_step: np.ndarray
+    cu_q: np.ndarray = None           # int32 [B+1] query rows of each sequence
     shared_blocks: int = 0            # physical blocks referenced by >1 seq
     notes: dict = field(default_factory=dict)
 
@@ -191,6 +206,8 @@ def make_workload(cfg: DecodeConfig, seed: int | None = None) -> Workload:
     MB = cfg.max_blocks_per_seq
 
     lens = _draw_lengths(cfg, rng)
+    nq = cfg.q_len
+    assert nq >= 1 and (nq == 1 or lens.min(initial=nq) >= nq), "each sequence holds its queries"
     nblk = -(-lens // bs)
 
     # Which leading tokens of each sequence are read from shared blocks.
@@ -201,7 +218,7 @@ def make_workload(cfg: DecodeConfig, seed: int | None = None) -> Workload:
         for members in groups:
             for i in members:
                 if lens[i] > 0:
-                    shared_len[i] = min(cfg.prefix_share, bs * ((lens[i] - 1) // bs))
+                    shared_len[i] = min(cfg.prefix_share, bs * ((lens[i] - cfg.q_len) // bs))
     else:
         groups = [[i] for i in range(B)]
 
@@ -234,31 +251,33 @@ def make_workload(cfg: DecodeConfig, seed: int | None = None) -> Workload:
             cursor += n_priv
             tables[i, :own_shared] = shared[:own_shared]
             tables[i, own_shared:own_shared + n_priv] = priv
-            # private fill rows: positions shared_len .. L-2
-            pos = np.arange(int(shared_len[i]), max(int(lens[i]) - 1, int(shared_len[i])))
+            # private fill rows: positions shared_len .. L-q_len-1
+            pos = np.arange(int(shared_len[i]), max(int(lens[i]) - nq, int(shared_len[i])))
             if pos.size:
                 fill_slot_parts.append(tables[i, pos // bs].astype(np.int64) * bs + pos % bs)
     assert cursor == demand
 
     fill_slots = (np.concatenate(fill_slot_parts) if fill_slot_parts
                   else np.zeros(0, dtype=np.int64)).astype(np.int64)
-    step_slots = np.full(B, -1, dtype=np.int64)
+    step_slots = np.full(B * nq, -1, dtype=np.int64)
     for i in range(B):
-        if lens[i] > 0:
-            p = int(lens[i]) - 1
-            step_slots[i] = int(tables[i, p // bs]) * bs + p % bs
+        for k in range(nq):
+            p = int(lens[i]) - nq + k
+            if p >= 0:
+                step_slots[i * nq + k] = int(tables[i, p // bs]) * bs + p % bs
 
-    q = _normals(rng, (B, Hq, D), cfg.q_std, cfg.q_dtype)
+    q = _normals(rng, (B * nq, Hq, D), cfg.q_std, cfg.q_dtype)
     Nf = fill_slots.size
     k_fill = _normals(rng, (Nf, Hkv, D), cfg.kv_std, cfg.src_dtype)
     v_fill = _normals(rng, (Nf, Hkv, D), cfg.kv_std, cfg.src_dtype)
-    k_step = _normals(rng, (B, Hkv, D), cfg.kv_std, cfg.src_dtype)
-    v_step = _normals(rng, (B, Hkv, D), cfg.kv_std, cfg.src_dtype)
+    k_step = _normals(rng, (B * nq, Hkv, D), cfg.kv_std, cfg.src_dtype)
+    v_step = _normals(rng, (B * nq, Hkv, D), cfg.kv_std, cfg.src_dtype)
 
     return Workload(cfg=cfg, context_lens=lens.astype(np.int32), block_tables=tables,
                     num_blocks=int(NB), q=q, fill_slots=fill_slots, k_fill=k_fill,
                     v_fill=v_fill, step_slots=step_slots, k_step=k_step, v_step=v_step,
-                    shared_blocks=shared_total, notes={"demand_blocks": demand})
+                    shared_blocks=shared_total, notes={"demand_blocks": demand},
+                    cu_q=(np.arange(B + 1) * nq).astype(np.int32))
 
 
 def algorithmic_bytes(cfg: DecodeConfig, context_lens: np.ndarray) -> int:
@@ -273,7 +292,7 @@ def algorithmic_bytes(cfg: DecodeConfig, context_lens: np.ndarray) -> int:
     T = int(lens.sum())
     nblk = int((-(-lens // cfg.block_size)).sum())
     kv = T * 2 * cfg.num_kv_heads * cfg.head_dim * esz[cfg.kv_dtype]
-    q = cfg.batch * cfg.num_q_heads * cfg.head_dim * esz[cfg.q_dtype]
+    q = cfg.batch * cfg.q_len * cfg.num_q_heads * cfg.head_dim * esz[cfg.q_dtype]
     tables = nblk * 4
     scales = nblk * cfg.num_kv_heads * 2 * 4 if cfg.kv_dtype == "i8" else 0
     return kv + q + tables + scales

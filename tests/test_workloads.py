@@ -13,6 +13,11 @@ SMALL = {
     "gqa8b_int8": variant(CONFIGS["gqa8b_int8"], batch=5, len_groups=((5, 1, 300),)),
     "skewed": variant(CONFIGS["skewed"], batch=10, max_len=9000,
                       len_groups=((3, 3000, 9000), (7, 16, 256))),
+    "spec_verify": variant(CONFIGS["spec_verify"], batch=7, len_groups=((7, 5, 600),)),
+    "prefill_chunk": variant(CONFIGS["prefill_chunk"], batch=3, q_len=40, max_len=700,
+                             len_groups=((3, 40, 700),)),
+    "skewed_q3": variant(CONFIGS["skewed"], batch=9, max_len=5000, q_len=3,
+                         len_groups=((2, 3000, 5000), (7, 16, 100))),
 }
 
 
@@ -26,20 +31,24 @@ def _check(w):
     for b in range(cfg.batch):
         assert np.all(t[b, :nblk[b]] >= 0) and np.all(t[b, :nblk[b]] < w.num_blocks)
         assert np.all(t[b, nblk[b]:] == -1)
+    nq = cfg.q_len
     written = set()
     for s in w.fill_slots.tolist():
         assert s not in written
         written.add(s)
+    assert w.cu_q.tolist() == [nq * b for b in range(cfg.batch + 1)]
+    assert w.q.shape[0] == cfg.batch * nq == w.step_slots.size
     for b in range(cfg.batch):
         if lens[b] == 0:
-            assert w.step_slots[b] == -1
+            assert np.all(w.step_slots[b * nq:(b + 1) * nq] == -1)
             continue
-        for p in range(int(lens[b]) - 1):
+        for p in range(int(lens[b]) - nq):
             assert int(t[b, p // bs]) * bs + p % bs in written
-        p = int(lens[b]) - 1
-        s = int(t[b, p // bs]) * bs + p % bs
-        assert w.step_slots[b] == s and s not in written
-    assert len(set(w.step_slots[w.step_slots >= 0].tolist())) == int((lens > 0).sum())
+        for k in range(nq):
+            p = int(lens[b]) - nq + k
+            s = int(t[b, p // bs]) * bs + p % bs
+            assert w.step_slots[b * nq + k] == s and s not in written
+    assert len(set(w.step_slots[w.step_slots >= 0].tolist())) == int(nq * (lens > 0).sum())
     return nblk
 
 
@@ -59,8 +68,9 @@ def test_generator_invariants(name):
         for blk, seqs in owner.items():
             if len(seqs) > 1:
                 assert len({s // cfg.share_group for s in seqs}) == 1
-        for b in range(cfg.batch):
-            assert owner[int(w.block_tables[b, nblk[b] - 1])] == {b}
+        for b in range(cfg.batch):   # blocks receiving new tokens are private
+            for p in range(int(w.context_lens[b]) - cfg.q_len, int(w.context_lens[b])):
+                assert owner[int(w.block_tables[b, p // 16])] == {b}
         assert w.shared_blocks > 0
     if cfg.num_blocks is None:
         assert w.num_blocks == -(-w.notes["demand_blocks"] * 11 // 10)
