@@ -47,9 +47,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--config", default="gqa8b", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--op", default="decode_step", choices=["decode_step", "copy_blocks"],
+    ap.add_argument("--op", default="decode_step",
+                    choices=["decode_step", "copy_blocks", "multiquery"],
                     help="decode_step: the hot path (default); copy_blocks: copy-on-write "
-                         "block copy of --copy-pairs random blocks of the workload's pool")
+                         "block copy of --copy-pairs random blocks of the workload's pool; "
+                         "multiquery: append of the q_len new tokens + causal multi-query "
+                         "attention (use --config spec_verify or prefill_chunk)")
     ap.add_argument("--copy-pairs", type=int, default=4096)
     ap.add_argument("--graph", action="store_true",
                     help="replay the step from a captured CUDA graph instead of eager launches")
@@ -540,12 +543,80 @@ def run_copy_blocks(args):
         "gpu_launches": args.steps}), flush=True)
 
 
+def run_multiquery(args):
+    """Speculative verification / prefill chunk step on 1 GPU."""
+    import torch
+    from paged_kv_decode_05_gb300 import binding as B
+    from paged_kv_decode_05_gb300.build import build
+    build()
+    device = torch.device("cuda", 0)
+    cfg = CONFIGS[args.config]
+    w = make_workload(cfg)
+    st = _gpu_state(w, device)
+    cu = torch.from_numpy(w.cu_q).to(device)
+    nq = cfg.q_len
+    ws = torch.empty(B.pkv_multiquery_workspace_size(cfg.batch, cfg.num_q_heads, nq,
+                                                     st["k_cache"], args.num_parts),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty_like(st["q"])
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        B.pkv_append(st["k_step"], st["v_step"], st["step_slots"], st["k_cache"], st["v_cache"],
+                     st["k_scales"], st["v_scales"], st["append_ws"], st["status"])
+        if ev is not None:
+            ev[1].record()
+        B.pkv_multiquery_attn(st["q"], cu, nq, st["k_cache"], st["v_cache"], st["block_tables"],
+                              st["context_lens"], cfg.softmax_scale, out, ws, args.num_parts,
+                              st["status"])
+        if ev is not None:
+            ev[2].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    evs = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+           for i in range(0, args.steps, max(1, args.event_every))}
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(args.steps):
+        step(evs.get(i))
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / args.steps
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs.values()) / len(evs)
+    alg = algorithmic_bytes(cfg, w.context_lens)
+    lens = w.context_lens.astype(np.int64)
+    # causal FLOPs: query i of a sequence attends to L - nq + i + 1 tokens, 4 D flops each head
+    flops = int(sum(4 * cfg.head_dim * cfg.num_q_heads * (nq * (L - nq) + nq * (nq + 1) // 2)
+                    for L in lens))
+    peak, src_name = load_peaks()
+    gbs = alg / (attn_ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "multi-query paged attention HBM GB/s (causal, q_len new tokens/sequence)",
+        "value": round(alg / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "dtype": cfg.kv_dtype, "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config, "q_len": nq,
+                   "algorithmic_bytes_per_step": alg, "attention_flops": flops},
+        "attn_ms_avg": round(attn_ms, 6), "attn_tflops": round(flops / (attn_ms / 1e3) / 1e12, 1),
+        "query_tokens_per_s": round(cfg.batch * nq / (ms / 1e3), 1),
+        "roofline": {"kernel": "mq_split_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": peak, "peak_source": src_name, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None},
+        "device_status": int(st["status"].item()),
+        "gpu_launches": args.steps * 3}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "copy_blocks":
         run_copy_blocks(args)
+    elif args.op == "multiquery":
+        run_multiquery(args)
     else:
         run_native(args)
 

@@ -187,6 +187,40 @@ pkv_status pkv_decode_combine(const pkv_cache_desc *cache, int32_t batch,
                               int32_t num_parts, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Multi-query attention: speculative verification and prefill chunks
+ *
+ * n_b = cu_q[b+1] - cu_q[b] new query tokens per sequence (already appended
+ * to the cache), causal among themselves: query i of sequence b sits at
+ * position L_b - n_b + i (L_b = context_lens[b]) and attends to positions
+ * 0 .. L_b - n_b + i. This is the target model scoring a draft's K tokens
+ * plus one in one batched pass (Continuous-Batching-LLM-Inference-Engine
+ * README, feature list "Speculative decoding") and a prefill chunk mixed into
+ * a continuous batch (mini-inference-engine overview). n_b = 1 everywhere is
+ * decode attention.
+ *
+ * q, out: [cu_q[batch], num_q_heads, head_dim], same dtype as the cache
+ * (PKV_F16 or PKV_BF16; INT8 caches are not supported here). cu_q: device
+ * int32 [batch+1], non-decreasing. max_q_len bounds every n_b; a sequence
+ * with n_b > max_q_len, n_b > L_b or L_b beyond its table is flagged
+ * PKV_DEV_BAD_LENGTH and its rows are not written. The g = num_q_heads /
+ * num_kv_heads query heads of each KV head and the n_b queries form the rows
+ * of a tensor-core tile. Supported: head_dim 64 or 128, g in {1, 2, 4},
+ * batch <= 4096. Workspace: pkv_multiquery_workspace_size with the same
+ * batch, num_q_heads, max_q_len, cache and num_parts (0 = one range per
+ * resident CTA); 256-byte aligned. Caches 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_q_len,
+                                     const pkv_cache_desc *cache, int32_t num_parts);
+
+pkv_status pkv_multiquery_attn(const void *q, pkv_dtype q_dtype, const int32_t *cu_q,
+                               int32_t max_q_len, const void *k_cache, const void *v_cache,
+                               const pkv_cache_desc *cache, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t batch, int32_t num_q_heads, float softmax_scale,
+                               void *out, void *workspace, size_t workspace_bytes,
+                               int32_t num_parts, uint32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Copy-on-write block copy (fork / rollback)
  *
  * Copies whole physical blocks src_blocks[i] -> dst_blocks[i] (all kv heads,

@@ -52,6 +52,10 @@ _SIGS = {
                                         _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_decode_combine": (ctypes.c_int, [_DESC, _I32, _I32, ctypes.c_int, _P, _P, _SZ, _I32, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _DESC, _P, _P, _I32, _P, _P]),
+    "pkv_multiquery_workspace_size": (_SZ, [_I32, _I32, _I32, _DESC, _I32]),
+    "pkv_multiquery_attn": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _DESC, _P, _I32,
+                                           _P, _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32,
+                                           _P, _P]),
     "pkv_decode_attn_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32,
                                                _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P]),
 }
@@ -191,6 +195,24 @@ def pkv_copy_blocks(k_cache, v_cache, src_blocks, dst_blocks, k_scales=None, v_s
                                  ctypes.byref(desc), _ptr(src_blocks), _ptr(dst_blocks),
                                  int(src_blocks.numel()), _ptr(dev_status), _stream(stream))
     _check("pkv_copy_blocks", code)
+
+
+def pkv_multiquery_workspace_size(batch, num_q_heads, max_q_len, k_cache, num_parts=0) -> int:
+    return int(lib().pkv_multiquery_workspace_size(batch, num_q_heads, max_q_len,
+                                                   ctypes.byref(cache_desc(k_cache)), num_parts))
+
+
+def pkv_multiquery_attn(q, cu_q, max_q_len, k_cache, v_cache, block_tables, context_lens,
+                        softmax_scale, out, workspace, num_parts=0, dev_status=None, stream=None):
+    """Causal attention of ``cu_q``-delimited new queries ``q [total_q, Hq, D]``."""
+    desc = cache_desc(k_cache)
+    code = lib().pkv_multiquery_attn(
+        _ptr(q), _dtype_code(q), _ptr(cu_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        int(cu_q.numel() - 1), int(q.shape[1]), float(softmax_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(num_parts), _ptr(dev_status),
+        _stream(stream))
+    _check("pkv_multiquery_attn", code)
 
 
 def pkv_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, out,

@@ -106,13 +106,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`.
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// of the global timer or 2^26 polls, whichever comes first (the poll cap
+// bounds the wait even if the timer were not to advance).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > limit_ns) return false;
+    for (uint32_t it = 1; !mbar_try_wait(bar, parity); ++it) {
+        if (it >= (1u << 26)) return false;
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

@@ -1,0 +1,134 @@
+"""GPU parity: pkv_multiquery_attn (speculative verification, prefill chunks)
+against the float64 causal oracle. Tolerance as for decode:
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise."""
+
+import numpy as np
+import pytest
+
+import oracle
+from _pkv_helpers import GpuCase, OracleCase, assert_attention_close, out_to_f64, to_dev
+from paged_kv_decode_05_gb300.workloads import CONFIGS, make_workload, variant
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_decode_05_gb300.build import build
+    build()
+
+
+def _sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+def run_mq(g, q, cu_q, max_q, num_parts=0):
+    import torch
+    from paged_kv_decode_05_gb300 import binding as B
+    cfg = g.cfg
+    qd = q if isinstance(q, torch.Tensor) else to_dev(q)
+    cu = cu_q if isinstance(cu_q, torch.Tensor) else to_dev(np.asarray(cu_q, np.int32))
+    out = torch.full(qd.shape, float("nan"), dtype=qd.dtype, device="cuda")
+    ws = torch.empty(B.pkv_multiquery_workspace_size(cfg.batch, cfg.num_q_heads, max_q, g.k_cache,
+                                                     num_parts), dtype=torch.uint8, device="cuda")
+    B.pkv_multiquery_attn(qd, cu, max_q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
+                          cfg.softmax_scale, out, ws, num_parts, g.status)
+    return out
+
+
+SMALL = {
+    "spec_verify": variant(CONFIGS["spec_verify"], batch=12, len_groups=((12, 5, 900),)),
+    "prefill_chunk": variant(CONFIGS["prefill_chunk"], batch=3, q_len=40, max_len=700,
+                             len_groups=((3, 40, 700),)),
+    "mha_q3_d64": variant(CONFIGS["mha7b"], batch=5, num_q_heads=4, num_kv_heads=4, head_dim=64,
+                          q_len=3, max_len=400, len_groups=((5, 3, 400),)),
+    "g2_q9_f16": variant(CONFIGS["gqa8b"], batch=6, num_q_heads=8, num_kv_heads=4,
+                         kv_dtype="f16", q_dtype="f16", src_dtype="f16", q_len=9,
+                         len_groups=((6, 9, 500),)),
+    "g4_q1": variant(CONFIGS["gqa8b"], batch=9, len_groups=((9, 1, 700),)),
+}
+_cache = {}
+
+
+def case(name):
+    if name not in _cache:
+        w = make_workload(SMALL[name])
+        g, o = GpuCase(w), OracleCase(w)
+        want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
+                                                 w.context_lens, w.cfg.softmax_scale)
+        _cache[name] = (w, g, o, want)
+    return _cache[name]
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("parts", [0, 1, 3, 17])
+def test_multiquery_small(name, parts):
+    w, g, o, want = case(name)
+    out = run_mq(g, w.q, w.cu_q, w.cfg.q_len, parts)
+    _sync()
+    assert_attention_close(out_to_f64(out), want, False, f"{name} parts={parts}")
+    assert int(g.status.item()) == 0
+
+
+def test_one_query_per_sequence_matches_decode_kernel():
+    import torch
+    w, g, o, want = case("g4_q1")
+    out = run_mq(g, w.q, w.cu_q, 1)
+    ref, _ = g.decode()
+    _sync()
+    a, b = out_to_f64(out), out_to_f64(ref)
+    assert_attention_close(a, want, False, "q_len 1")
+    assert np.abs(a - b).max() < 2e-2
+
+
+def test_variable_query_counts_including_empty():
+    w, g, o, _ = case("prefill_chunk")
+    rng = np.random.default_rng(5)
+    qmax = w.cfg.q_len
+    ns = np.array([0, 17, qmax], np.int32)[: w.cfg.batch]
+    rng.shuffle(ns)
+    rows = [w.q[b * qmax: b * qmax + int(ns[b])] for b in range(w.cfg.batch)]
+    qv = np.concatenate(rows)
+    cu = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    want = oracle.paged_multiquery_attention(qv, cu, o.k, o.v, w.block_tables, w.context_lens,
+                                             w.cfg.softmax_scale)
+    for parts in (0, 2, 9):
+        out = run_mq(g, qv, cu, qmax, parts)
+        _sync()
+        assert_attention_close(out_to_f64(out), want, False, f"varlen parts={parts}")
+
+
+def test_too_many_queries_are_flagged_not_written():
+    import torch
+    from paged_kv_decode_05_gb300 import binding as B
+    w, g, o, _ = case("spec_verify")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g_status, g.status = g.status, status
+    try:
+        out = run_mq(g, w.q, w.cu_q, w.cfg.q_len - 1)   # max_q_len below the real n_b
+        _sync()
+    finally:
+        g.status = g_status
+    assert int(status.item()) & B.DEV_BAD_LENGTH
+    assert torch.isnan(out.float()).all()            # nothing written
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["spec_verify", "prefill_chunk"])
+def test_multiquery_full_size_sampled(name):
+    w = make_workload(CONFIGS[name])
+    g, o = GpuCase(w), OracleCase(w)
+    lens = w.context_lens
+    order = np.argsort(lens)
+    seqs = sorted(set(order[:2].tolist() + order[-2:].tolist() +
+                      np.linspace(0, w.cfg.batch - 1, min(8, w.cfg.batch)).astype(int).tolist()))
+    want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables, lens,
+                                             w.cfg.softmax_scale, seqs=seqs)
+    out = run_mq(g, w.q, w.cu_q, w.cfg.q_len)
+    _sync()
+    got = out_to_f64(out)
+    rows = np.concatenate([np.arange(w.cu_q[b], w.cu_q[b + 1]) for b in seqs])
+    assert_attention_close(got[rows], want, False, name)
+    assert np.isfinite(got).all()
+    assert int(g.status.item()) == 0
