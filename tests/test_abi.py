@@ -110,3 +110,39 @@ def test_workspace_size_formula(lib):
     a = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert got == a(4 * 257) + a(slots * 4 * 2 * 4) + a(slots * 4 * 128 * 4)
     assert lib.pkv_decode_workspace_size(256, 12, ctypes.byref(d), 64) == 0  # unsupported group
+
+
+def test_multiquery_and_copy_blocks_host_validation(lib):
+    fake = 0x100000
+    d = desc(nb=64, h=2, d=128)
+
+    def mq(q_dtype=B.PKV_BF16, dd=None, batch=4, hq=8, max_q=5, ws=fake, ws_bytes=1 << 30,
+           parts=16):
+        return lib.pkv_multiquery_attn(fake, q_dtype, fake, max_q, fake, fake,
+                                       ctypes.byref(dd or d), fake, 4, fake, batch, hq, 0.125,
+                                       fake, ws, ws_bytes, parts, None, None)
+    assert mq(hq=7) == 1                         # heads not a multiple of kv heads
+    assert mq(hq=16) == 2                        # group 8 not built
+    assert mq(max_q=0) == 1
+    assert mq(q_dtype=B.PKV_F16) == 1            # q dtype must match the cache
+    assert mq(dd=desc(dt=B.PKV_I8)) == 2         # INT8 caches not supported here
+    assert mq(dd=desc(d=96)) == 2
+    assert mq(batch=5000) == 2
+    assert mq(batch=0) == 0
+    assert mq(ws_bytes=64) == 3
+    assert mq(ws=fake + 128) == 3                # workspace not 256-aligned
+    # size query agrees with the layout: rows per tile 32 (20 rows), one tile
+    dd = desc(nb=64, h=2, d=128)
+    slots = 4 * 2 * 1 + 16
+    a = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert lib.pkv_multiquery_workspace_size(4, 8, 5, ctypes.byref(dd), 16) == \
+        a(4 * 5) + a(slots * 32 * 2 * 4) + a(slots * 32 * 128 * 4)
+    # block copy
+    assert lib.pkv_copy_blocks(fake, fake, None, None, ctypes.byref(d), fake, fake, 0, None,
+                               None) == 0
+    assert lib.pkv_copy_blocks(fake, fake, None, None, ctypes.byref(d), fake, fake, -1, None,
+                               None) == 1
+    assert lib.pkv_copy_blocks(fake, fake, None, None, ctypes.byref(desc(dt=B.PKV_I8)), fake, fake,
+                               3, None, None) == 1   # INT8 needs scales
+    assert lib.pkv_copy_blocks(fake + 4, fake, None, None, ctypes.byref(d), fake, fake, 3, None,
+                               None) == 1            # misaligned cache
