@@ -253,34 +253,36 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 
     if (warp == NW) {
         // ------------------------------------------------------ producer ---
-        auto fetch = [&](int base, int& b, int& kvh, int& t, int& j, int& n, int& L, int& blk) {
+        auto fetch = [&](int base, int& b, int& kvh, int& t, int& j, int& n, int& L, int& blk,
+                         int& cu) {
             const int u = base + lane;
             if (u < u1) {
                 mq_decode_unit(p, prefix, u, C::RT, G, b, kvh, t, j, n, L);
                 blk = __ldg(p.block_tables + (long long)b * p.mb + j);
+                cu = __ldg(p.cu_q + b);
             } else {
-                b = kvh = t = j = n = L = 0;
+                b = kvh = t = j = n = L = cu = 0;
                 blk = -1;
             }
         };
         int cbase = u0;
-        int cb, ck, ct, cj, cn, cL, cblk, xb, xk, xt, xj, xn, xL, xblk;
-        fetch(cbase, cb, ck, ct, cj, cn, cL, cblk);
-        fetch(cbase + 32, xb, xk, xt, xj, xn, xL, xblk);
+        int cb, ck, ct, cj, cn, cL, cblk, ccu, xb, xk, xt, xj, xn, xL, xblk, xcu;
+        fetch(cbase, cb, ck, ct, cj, cn, cL, cblk, ccu);
+        fetch(cbase + 32, xb, xk, xt, xj, xn, xL, xblk, xcu);
         uint32_t parity = 0;
         int s = 0;
         for (int u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1) {
             int idx = u - cbase;
             if (idx >= 32) {
                 cbase += 32;
-                cb = xb; ck = xk; ct = xt; cj = xj; cn = xn; cL = xL; cblk = xblk;
-                fetch(cbase + 32, xb, xk, xt, xj, xn, xL, xblk);
+                cb = xb; ck = xk; ct = xt; cj = xj; cn = xn; cL = xL; cblk = xblk; ccu = xcu;
+                fetch(cbase + 32, xb, xk, xt, xj, xn, xL, xblk, xcu);
                 idx -= 32;
             }
             const int b = __shfl_sync(kFull, cb, idx), kvh = __shfl_sync(kFull, ck, idx);
             const int t = __shfl_sync(kFull, ct, idx), j = __shfl_sync(kFull, cj, idx);
             const int n = __shfl_sync(kFull, cn, idx), L = __shfl_sync(kFull, cL, idx);
-            const int blk = __shfl_sync(kFull, cblk, idx);
+            const int blk = __shfl_sync(kFull, cblk, idx), cu = __shfl_sync(kFull, ccu, idx);
             if (u - u0 >= NS) {  // wait until every consumer released this stage
                 const bool ok = mbar_wait_bounded(smem_addr(&empty[s]), (parity >> s) & 1u, kMqWaitNs);
                 parity ^= 1u << s;
@@ -293,7 +295,8 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 const uint32_t bar = smem_addr(&full[s]);
                 const bool valid = unsigned(blk) < unsigned(p.num_blocks);
                 meta[2 * s] = make_int4(b, kvh, t, j);
-                meta[2 * s + 1] = make_int4(n, L, valid ? 1 : 0, (u == u0 || j == 0) ? 1 : 0);
+                // (n, L, cu_q[b], flags: bit 0 = block valid, bit 1 = first unit of a piece)
+                meta[2 * s + 1] = make_int4(n, L, cu, (valid ? 1 : 0) | ((u == u0 || j == 0) ? 2 : 0));
                 if (valid) {
                     const int y = (blk * p.hkv + kvh) * kBlockSize;
                     unsigned char* st = smem + s * C::STAGE;
@@ -366,7 +369,7 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             break;
         }
         const int4 ma = meta[2 * s], mb = meta[2 * s + 1];
-        if (mb.w) {  // first unit of a new piece: load the warp's Q rows
+        if (mb.w & 2) {  // first unit of a new piece: load the warp's Q rows
             if (pb >= 0) finalize();
             pb = ma.x; pk = ma.y; pt = ma.z; first_j = ma.w; pn = mb.x; pL = mb.y;
             const int rr0 = pt * C::RT + warp * 16 + gq, rr1 = rr0 + 8;
@@ -375,7 +378,7 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             // warp-uniform: the collective ldmatrix / mma / shuffles below
             // must be reached by all 32 lanes or by none
             wact = pt * C::RT + warp * 16 < pn * G;
-            const int cu = p.cu_q[pb];
+            const int cu = mb.z;
             orow0 = ((long long)(cu + rr0 / G) * p.hq + pk * G + rr0 % G) * D;
             orow1 = ((long long)(cu + rr1 / G) * p.hq + pk * G + rr1 % G) * D;
             pos0 = pL - pn + rr0 / G;
@@ -395,7 +398,7 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         }
         last_j = ma.w;
         bool zeroed = false;
-        if (mb.z && wact) {
+        if ((mb.w & 1) && wact) {
             unsigned char* kt = smem + s * C::STAGE;
             unsigned char* vt = kt + C::TILE;
             const int j = ma.w;
