@@ -54,6 +54,9 @@ def parse_args(argv=None):
                          "multiquery: append of the q_len new tokens + causal multi-query "
                          "attention (use --config spec_verify or prefill_chunk)")
     ap.add_argument("--copy-pairs", type=int, default=4096)
+    ap.add_argument("--unfused", action="store_true",
+                    help="step = pkv_append + split + combine (3 launches) instead of the "
+                         "fused pkv_decode_step (split with the append folded in + combine)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step from a captured CUDA graph instead of eager launches")
     ap.add_argument("--num-parts", type=int, default=0, help="worker warps (0 = device default)")
@@ -267,22 +270,34 @@ def _gpu_state(w, device):
     return st
 
 
-def _step(st, cfg, ws, parts, ev=None):
-    """One decode step: append the new token, split, combine (3 or 6 launches).
+def _step(st, cfg, ws, parts, ev=None, fused=None):
+    """One decode step: the new token's cache write, split, combine.
 
-    ``ev``: optional 4 CUDA events recorded before the append, between append
-    and split, between split and combine, and after the combine.
+    Unfused: pkv_append, pkv_decode_split, pkv_decode_combine (3 launches; 6
+    for INT8). Fused (16-bit caches): pkv_decode_step's split phase writes the
+    new rows itself, then pkv_decode_combine (2 launches).
+    ``ev``: optional 4 CUDA events recorded before the append, before the
+    split, before the combine and after it (the first two coincide if fused).
     """
     from paged_kv_decode_05_gb300 import binding as B
+    if fused is None:
+        fused = st.get("fused", False)
     if ev is not None:
         ev[0].record()
-    B.pkv_append(st["k_step"], st["v_step"], st["step_slots"], st["k_cache"], st["v_cache"],
-                 st["k_scales"], st["v_scales"], st["append_ws"], st["status"])
+    if not fused:
+        B.pkv_append(st["k_step"], st["v_step"], st["step_slots"], st["k_cache"],
+                     st["v_cache"], st["k_scales"], st["v_scales"], st["append_ws"],
+                     st["status"])
     if ev is not None:
         ev[1].record()
-    B.pkv_decode_split(st["q"], st["k_cache"], st["v_cache"], st["block_tables"],
-                       st["context_lens"], cfg.softmax_scale, st["out"], ws, st["k_scales"],
-                       st["v_scales"], parts, st["status"])
+    if fused:
+        B.pkv_decode_step(st["q"], st["k_step"], st["v_step"], st["k_cache"], st["v_cache"],
+                          st["block_tables"], st["context_lens"], cfg.softmax_scale, st["out"],
+                          ws, parts, st["status"], run_combine=False)
+    else:
+        B.pkv_decode_split(st["q"], st["k_cache"], st["v_cache"], st["block_tables"],
+                           st["context_lens"], cfg.softmax_scale, st["out"], ws,
+                           st["k_scales"], st["v_scales"], parts, st["status"])
     if ev is not None:
         ev[2].record()
     B.pkv_decode_combine(st["out"], st["k_cache"], ws, parts)
@@ -313,7 +328,8 @@ def run_native(args):
     ws = torch.empty(B.pkv_decode_workspace_size(cfg.batch, cfg.num_q_heads, st["k_cache"], parts),
                      dtype=torch.uint8, device=device)
     alg = algorithmic_bytes(cfg, w.context_lens)
-    launches_per_step = 6 if cfg.kv_dtype == "i8" else 3
+    st["fused"] = (not args.unfused) and cfg.kv_dtype != "i8"
+    launches_per_step = 2 if st["fused"] else (6 if cfg.kv_dtype == "i8" else 3)
     K, W = args.steps, args.warmup
 
     for _ in range(W):
@@ -383,7 +399,10 @@ def run_native(args):
                    "algorithmic_bytes_per_step": alg, "workers": parts,
                    "l2": "no flush: the KV cache read each step (%.2f GB) is far larger than "
                          "the 129 MB L2" % (alg / 1e9),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "step": ("pkv_decode_step split phase (new K/V rows written by the split "
+                            "kernel) + pkv_decode_combine" if st["fused"] else
+                            "pkv_append + pkv_decode_split + pkv_decode_combine")},
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peak, 2),
         "decode_tokens_per_s": round(cfg.batch * world / step_s, 1),

@@ -51,6 +51,9 @@ _SIGS = {
     "pkv_decode_split": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
                                         _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_decode_combine": (ctypes.c_int, [_DESC, _I32, _I32, ctypes.c_int, _P, _P, _SZ, _I32, _P]),
+    "pkv_decode_step": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
+                                       _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _I32, _P,
+                                       _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _DESC, _P, _P, _I32, _P, _P]),
     "pkv_multiquery_workspace_size": (_SZ, [_I32, _I32, _I32, _DESC, _I32]),
     "pkv_multiquery_attn": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _DESC, _P, _I32,
@@ -175,6 +178,21 @@ def pkv_decode_split(q, k_cache, v_cache, block_tables, context_lens, softmax_sc
                      stream=None):
     _decode("pkv_decode_split", q, k_cache, v_cache, block_tables, context_lens, softmax_scale,
             out, workspace, k_scales, v_scales, num_parts, dev_status, stream)
+
+
+def pkv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, softmax_scale,
+                    out, workspace, num_parts=0, dev_status=None, stream=None, run_combine=True):
+    """Write ``k_new/v_new [B, Hkv, D]`` at each sequence's last position, then attend
+    (``run_combine=False``: split phase only; :func:`pkv_decode_combine` must follow)."""
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    code = lib().pkv_decode_step(
+        _ptr(q), _dtype_code(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        B, Hq, float(softmax_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(num_parts), int(bool(run_combine)),
+        _ptr(dev_status), _stream(stream))
+    _check("pkv_decode_step", code)
 
 
 def pkv_decode_combine(out, k_cache, workspace, num_parts=0, stream=None):

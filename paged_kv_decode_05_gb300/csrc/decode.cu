@@ -105,6 +105,8 @@ struct DecodeParams {
     float* part_ml;       // [slots, G, 2]
     int32_t* ws_prefix;   // [batch + 1] copy of the block prefix for the combine
     uint32_t* status;
+    const void* k_new;    // fused decode step: [batch, hkv, D] rows for position L - 1
+    const void* v_new;    // (nullptr: attention only)
     int batch, hq, hkv, mb, num_blocks, workers;
     float qscale;         // softmax_scale * log2(e)
 };
@@ -316,8 +318,19 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
             const uint32_t bar = smem_addr(&bars[s]);
             const bool ok = unsigned(blk) < unsigned(p.num_blocks);
             const bool first = (u == u0) || (j == 0);   // first unit of a piece
-            meta[s] = make_int4(b, kvh | ((ok ? 1 : 0) << 16) | ((first ? 1 : 0) << 17), j, len);
-            const uint32_t tx = (ok ? 2 * C::TILE : 0) + (first ? C::QBYTES : 0);
+            // Fused decode step: the tile holding the sequence's new token
+            // (position len - 1, row r) takes rows [0, r) from the cache and
+            // row r from k_new / v_new; the consumer then stores row r into
+            // the cache. Rows past r are masked, so they are not copied.
+            const bool fuse = !C::kI8 && ok && p.k_new != nullptr && len > 0 &&
+                              j == (len - 1) / kBlockSize &&
+                              __ldg(p.context_lens + b) == len;   // not clamped: flagged, no write
+            const int r = fuse ? (len - 1) % kBlockSize : kBlockSize;
+            meta[s] = make_int4(b, kvh | ((ok ? 1 : 0) << 16) | ((first ? 1 : 0) << 17) |
+                                       ((fuse ? 1 : 0) << 18), j, len);
+            if (fuse) scl[s].x = __int_as_float(blk);   // scales are unused for 16-bit caches
+            const uint32_t tx = (ok ? 2 * (fuse ? (r + 1) * C::ROW : C::TILE) : 0) +
+                                (first ? C::QBYTES : 0);
             if (tx) mbar_arrive_expect_tx(bar, tx);
             else mbar_arrive(bar);
             if (first)
@@ -327,10 +340,19 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
             if (ok) {
                 const long long tile = (long long)blk * p.hkv + kvh;
                 unsigned char* st = region + s * C::STAGE;
-                bulk_g2s(smem_addr(st), static_cast<const char*>(p.k_cache) + tile * C::TILE,
-                         C::TILE, bar);
-                bulk_g2s(smem_addr(st + C::TILE),
-                         static_cast<const char*>(p.v_cache) + tile * C::TILE, C::TILE, bar);
+                if (r > 0) {
+                    bulk_g2s(smem_addr(st), static_cast<const char*>(p.k_cache) + tile * C::TILE,
+                             r * C::ROW, bar);
+                    bulk_g2s(smem_addr(st + C::TILE),
+                             static_cast<const char*>(p.v_cache) + tile * C::TILE, r * C::ROW, bar);
+                }
+                if (fuse) {
+                    const long long src = ((long long)b * p.hkv + kvh) * C::ROW;
+                    bulk_g2s(smem_addr(st + r * C::ROW), static_cast<const char*>(p.k_new) + src,
+                             C::ROW, bar);
+                    bulk_g2s(smem_addr(st + C::TILE + r * C::ROW),
+                             static_cast<const char*>(p.v_new) + src, C::ROW, bar);
+                }
                 if constexpr (C::kI8) {
                     cp_async_4(smem_addr(&scl[s].x), p.k_scales + tile);
                     cp_async_4(smem_addr(&scl[s].y), p.v_scales + tile);
@@ -477,6 +499,21 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
         if (flags & 1) {
             const unsigned char* kt = region + s * C::STAGE;
             const unsigned char* vt = kt + C::TILE;
+            if constexpr (!C::kI8) {
+                if (flags & 4) {   // fused step: the new token's row goes to the cache
+                    const int r = (mt.w - 1) % kBlockSize;
+                    const long long tile = (long long)__float_as_int(scl[s].x) * p.hkv + (mt.y & 0xffff);
+                    const long long dst = (tile * C::TILE + r * C::ROW) / 4;
+                    const uint32_t* ks = reinterpret_cast<const uint32_t*>(kt + r * C::ROW);
+                    const uint32_t* vs = reinterpret_cast<const uint32_t*>(vt + r * C::ROW);
+                    uint32_t* kd = static_cast<uint32_t*>(const_cast<void*>(p.k_cache)) + dst;
+                    uint32_t* vd = static_cast<uint32_t*>(const_cast<void*>(p.v_cache)) + dst;
+                    for (int wv = lane; wv < C::ROW / 4; wv += 32) {
+                        kd[wv] = ks[wv];
+                        vd[wv] = vs[wv];
+                    }
+                }
+            }
             const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
             float ksc = 1.f, vsc = 1.f;
             if constexpr (C::kI8) {
@@ -848,7 +885,8 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
                       const int32_t* block_tables, int32_t mb, const int32_t* context_lens,
                       int32_t batch, int32_t hq, float softmax_scale, void* out, void* workspace,
                       size_t workspace_bytes, int32_t num_parts, uint32_t* dev_status,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, const void* k_new = nullptr,
+                      const void* v_new = nullptr) {
     Ops ops;
     int G = 0;
     pkv_status s = check_decode(cache, batch, hq, q_dtype, &ops, &G);
@@ -887,6 +925,8 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
         p.part_ml = reinterpret_cast<float*>(ws + l.ml_off);
         p.ws_prefix = reinterpret_cast<int32_t*>(ws + l.prefix_off);
         p.status = dev_status;
+        p.k_new = k_new;
+        p.v_new = v_new;
         p.batch = batch; p.hq = hq; p.hkv = hkv; p.mb = mb; p.num_blocks = cache->num_blocks;
         p.workers = int(workers);
         p.qscale = softmax_scale * kLog2e;
@@ -961,6 +1001,25 @@ extern "C" pkv_status pkv_decode_split(const void* q, pkv_dtype q_dtype, const v
     return run_decode(true, false, q, q_dtype, k_cache, v_cache, k_scales, v_scales, cache,
                       block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
                       softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream);
+}
+
+extern "C" pkv_status pkv_decode_step(const void* q, pkv_dtype q_dtype, const void* k_new,
+                                      const void* v_new, void* k_cache, void* v_cache,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                      int32_t batch, int32_t num_q_heads, float softmax_scale,
+                                      void* out, void* workspace, size_t workspace_bytes,
+                                      int32_t num_parts, int32_t run_combine,
+                                      uint32_t* dev_status, cudaStream_t stream) {
+    if (!cache) return PKV_ERR_INVALID_ARG;
+    if (cache->kv_dtype == PKV_I8) return PKV_ERR_UNSUPPORTED;
+    if (run_combine != 0 && run_combine != 1) return PKV_ERR_INVALID_ARG;
+    if (batch > 0 && (!k_new || !v_new || !is_aligned(k_new, 16) || !is_aligned(v_new, 16)))
+        return PKV_ERR_INVALID_ARG;
+    return run_decode(true, run_combine == 1, q, q_dtype, k_cache, v_cache, nullptr, nullptr, cache,
+                      block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                      softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream,
+                      k_new, v_new);
 }
 
 extern "C" pkv_status pkv_decode_combine(const pkv_cache_desc* cache, int32_t batch,
