@@ -44,6 +44,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// a if c else b, per 32-bit word (lane-dependent register selection)
+__device__ __forceinline__ uint4 sel4(bool c, const uint4& a, const uint4& b) {
+    return make_uint4(c ? a.x : b.x, c ? a.y : b.y, c ? a.z : b.z, c ? a.w : b.w);
+}
+
 template <typename KV, int D, int G>
 struct Cfg {
     static constexpr int esize = Elem<KV>::bytes;
@@ -55,16 +60,8 @@ struct Cfg {
     // that 3 CTAs of 4 warps share an SM (at least 2 stages).
     static constexpr int QBYTES = G * D * 2;   // q rows of one (sequence, kv head)
     static constexpr int NS = (19456 / (STAGE + QBYTES)) < 2 ? 2 : (19456 / (STAGE + QBYTES));
-    // QK mapping: 8 lanes per token row, 4 rows per pass, 4 passes.
-    static constexpr int E = D / 8;                               // elements per lane per row
-    static constexpr int VB = (E * esize) < 16 ? (E * esize) : 16;  // bytes per vector load
-    static constexpr int NV = E * esize / VB;                     // vector loads per row
-    static constexpr int EV = VB / esize;                         // elements per vector
-    // P.V mapping: each lane owns D/32 output dims.
+    // INT8 P.V on the CUDA cores: each lane owns D/32 output dims.
     static constexpr int DPL = D / 32;
-    // Exchange-halving reduction of 4*G partial dots over 8 lanes.
-    static constexpr int NVAL = 4 * G;
-    static constexpr int NF = NVAL >= 8 ? NVAL / 8 : 1;          // scores per lane afterwards
     // Per-warp shared-memory region.
     static constexpr int OFF_BAR = NS * STAGE;                       // 8-byte mbarriers
     static constexpr int OFF_META = align_up(OFF_BAR + NS * 8, 16);   // int4 per stage
@@ -75,7 +72,6 @@ struct Cfg {
     static constexpr int WARP_BYTES = align_up(OFF_Q + NS * QBYTES, 128);
     static_assert(NS >= 2 && NS <= 32, "stage count (one parity bit per stage)");
     static_assert(STAGE % 128 == 0 && OFF_Q % 128 == 0 && QBYTES % 16 == 0, "copy alignment");
-    static_assert(E % EV == 0 && EV % 2 == 0 && NV >= 1, "lane element layout");
     static_assert(G == 1 || G == 2 || G == 4, "group size");
 };
 
@@ -166,41 +162,6 @@ __device__ __forceinline__ void decode_unit(long long u, const int* prefix, int 
     j = r - kvh * nb;
 }
 
-// One exchange-halving step over lane bit `bit`: N values -> N/2 values
-// (each summed with the partner lane's), or a butterfly when N == 1.
-template <int N>
-__device__ __forceinline__ void xstep(float* v, int bit, int lane, int& base) {
-    if constexpr (N >= 2) {
-        const bool hi = (lane & bit) != 0;
-#pragma unroll
-        for (int i = 0; i < N / 2; ++i) {
-            const float keep = hi ? v[i + N / 2] : v[i];
-            const float send = hi ? v[i] : v[i + N / 2];
-            v[i] = keep + __shfl_xor_sync(kFull, send, bit);
-        }
-        if (hi) base += N / 2;
-    } else {
-        v[0] += __shfl_xor_sync(kFull, v[0], bit);
-    }
-}
-
-// Load NPAIR pairs of 16-bit values starting at element `off` (16-byte
-// aligned) of a shared-memory row block as float2, times `scale`.
-template <typename QT, int NPAIR>
-__device__ __forceinline__ void load_q_pairs(const void* q, int off, float scale, float2* dst) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + off);
-#pragma unroll
-    for (int v = 0; v < NPAIR / 4; ++v) {
-        const uint4 x = src[v];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = unpack2(QT{}, w[i]);
-            dst[v * 4 + i] = make_float2(f.x * scale, f.y * scale);
-        }
-    }
-}
-
 // Raw words of one vector load from shared memory -> float2 pairs.
 template <typename KV, int VB>
 __device__ __forceinline__ void load_pairs_smem(const unsigned char* src, float2* dst) {
@@ -253,12 +214,19 @@ __device__ __forceinline__ void store_out(void* out, long long off, const float2
         }
     }
     uint16_t* dst = static_cast<uint16_t*>(out) + off;
-    if constexpr (DPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-    else *reinterpret_cast<uint32_t*>(dst) = w[0];
+    if constexpr (DPL % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < DPL / 8; ++i)
+            reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else if constexpr (DPL == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = w[0];
+    }
 }
 
 template <typename KV, typename QT, int D, int G>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeParams p) {
     using C = Cfg<KV, D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
     int* prefix = reinterpret_cast<int*>(smem) + 4;
@@ -365,72 +333,116 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
         }
     };
 
-    // ---- consumer state: the lane's token and heads after the reduction
-    const int rgrp = lane >> 3, r8 = lane & 7;
-    int xbase = 0;
-    {
-        int n = C::NVAL;
-        for (int bit = 4; bit; bit >>= 1) {
-            if (n >= 2) {
-                if (lane & bit) xbase += n / 2;
-                n /= 2;
-            }
-        }
-    }
-    const int my_t = rgrp + 4 * (xbase / G);      // token row of the lane's scores
-    const int h0 = xbase % G;                     // first head of the lane's scores
-    const bool dup = (G == 1) && (lane & 1);      // G == 1: lane pairs hold one score
-
-    // INT8 caches compute scores on the tensor cores (mma.sync m16n8k16, K
-    // codes exact in fp16, fp32 accumulators): rows = the tile's 16 tokens,
-    // columns = the g heads (padded to 8). Lane (gq, tq) = (lane / 4, lane % 4)
-    // then holds tokens gq and gq + 8 of heads 2tq and 2tq + 1.
-    constexpr bool kMma = C::kI8;
-    constexpr int LS = kMma ? 2 : C::NF;         // lane partial sums of l
+    // ---- consumer: both paths score on the tensor cores (mma.sync m16n8k16,
+    // fp32 accumulators) with rows = the tile's 16 tokens and columns = the g
+    // heads (padded to 8). Lane (gq, tq) = (lane / 4, lane % 4) then holds
+    // tokens gq and gq + 8 of heads 2tq and 2tq + 1.
+    //  * 16-bit caches: P.V also runs on the tensor cores as
+    //    O^T[dims x heads] += V^T[dims x 16 tokens] P^T[16 tokens x heads]; lane
+    //    (gq, tq) accumulates dims [gq*D/8, (gq+1)*D/8) of heads 2tq, 2tq + 1,
+    //    so its softmax state is that of its own two heads.
+    //  * INT8 caches: K codes become fp16 exactly for the scores; P.V on the
+    //    CUDA cores, each lane owning D/32 output dims of every head.
+    constexpr bool k16 = !C::kI8;
+    constexpr int MT = D / 16;                   // m-tiles of P.V (16-bit path)
+    constexpr int DL = D / 8;                    // dims a lane row group owns
     const int gq = lane >> 2, tq = lane & 3;
-    float2 q2[kMma ? 1 : G][kMma ? 1 : C::E / 2];
-    uint32_t qb[kMma ? D / 16 : 1][2];           // fp16x2 B fragments of q
-    float m[G], lsum[LS];
-    float2 o2[G][C::DPL / 2];
+    uint32_t qb[D / 16][2];                      // B fragments of q, per k-step
+    float m[k16 ? 2 : G], lsum[2] = {0.f, 0.f};
+    float oa[k16 ? MT : 1][4];                   // 16-bit: O^T accumulators
+    float2 o2[k16 ? 1 : G][k16 ? 1 : C::DPL / 2];  // INT8: per-head output dims
     int pb = -1, pkvh = -1, first_j = 0, last_j = 0, plen = 0;
 
-    // Does this lane's lsum hold a partial of head hh, and at which index?
-    auto owns = [&](int hh) -> bool {
-        if constexpr (kMma) return (hh >> 1) == tq;
-        else return hh / C::NF == h0 / C::NF && !dup;
-    };
-    auto lidx = [&](int hh) -> int { return kMma ? (hh & 1) : hh % C::NF; };
+    // Does this lane's lsum hold a partial of head hh (INT8 path), and where?
+    auto owns = [&](int hh) -> bool { return (hh >> 1) == tq; };
+    auto lidx = [&](int hh) -> int { return hh & 1; };
 
     auto finalize = [&]() {
-        float lh[G];
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) lh[hh] = owns(hh) ? lsum[lidx(hh)] : 0.f;
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) lh[hh] += __shfl_xor_sync(kFull, lh[hh], off);
         const int nbk = prefix[pb + 1] - prefix[pb];
         const long long seg = (long long)pb * p.hkv + pkvh;
-        if (first_j == 0 && last_j == nbk - 1) {
+        const bool whole = (first_j == 0 && last_j == nbk - 1);
+        if constexpr (k16) {
+            float lh[2] = {lsum[0], lsum[1]};
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
-                const long long off = ((long long)pb * p.hq + pkvh * G + h) * D + lane * C::DPL;
-                store_out<QT, C::DPL>(p.out, off, o2[h], inv);
+            for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) lh[e] += __shfl_xor_sync(kFull, lh[e], off);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = 2 * tq + e;
+                if (h >= G) continue;
+                if (whole) {
+                    float2 v[MT];
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) v[mt] = make_float2(oa[mt][e], oa[mt][2 + e]);
+                    const float inv = lh[e] > 0.f ? 1.0f / lh[e] : 0.f;
+                    store_out<QT, DL>(p.out, ((long long)pb * p.hq + pkvh * G + h) * D + gq * DL, v,
+                                      inv);
+                } else {
+                    const long long slot = seg + w;
+                    float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * G + h) * D + gq * DL);
+#pragma unroll
+                    for (int i = 0; i < MT / 2; ++i)
+                        dst[i] = make_float4(oa[2 * i][e], oa[2 * i][2 + e], oa[2 * i + 1][e],
+                                             oa[2 * i + 1][2 + e]);
+                    if (gq == 0)
+                        *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) =
+                            make_float2(m[e], lh[e]);
+                }
             }
         } else {
-            const long long slot = seg + w;
+            float lh[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float* dst = p.part_o + ((slot * G + h) * D + lane * C::DPL);
-                if constexpr (C::DPL == 4)
-                    *reinterpret_cast<float4*>(dst) =
-                        make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
-                else
-                    *reinterpret_cast<float2*>(dst) = o2[h][0];
-                if (lane == 0)
-                    *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) =
-                        make_float2(m[h], lh[h]);
+            for (int hh = 0; hh < G; ++hh) lh[hh] = owns(hh) ? lsum[lidx(hh)] : 0.f;
+#pragma unroll
+            for (int off = 16; off; off >>= 1)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) lh[hh] += __shfl_xor_sync(kFull, lh[hh], off);
+            if (whole) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
+                    const long long off = ((long long)pb * p.hq + pkvh * G + h) * D + lane * C::DPL;
+                    store_out<QT, C::DPL>(p.out, off, o2[h], inv);
+                }
+            } else {
+                const long long slot = seg + w;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float* dst = p.part_o + ((slot * G + h) * D + lane * C::DPL);
+                    if constexpr (C::DPL == 4)
+                        *reinterpret_cast<float4*>(dst) =
+                            make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
+                    else
+                        *reinterpret_cast<float2*>(dst) = o2[h][0];
+                    if (lane == 0)
+                        *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) =
+                            make_float2(m[h], lh[h]);
+                }
+            }
+        }
+    };
+
+    uint32_t vw[k16 ? 4 : 1][k16 ? DL / 2 : 1];   // V fragments of the current unit
+    // V fragments of the unit in stage s: rows 2tq, 2tq + 1, 2tq + 8, 2tq + 9,
+    // the lane row group's DL dims (16-bit path)
+    auto load_v = [&](const unsigned char* vt) {
+        // V: lanes of odd tq read a row's two 16-byte chunks in the
+        // other order (halves the bank conflicts of the four rows)
+        const int vswap = (DL / 8 == 2) ? (tq & 1) : 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
+            const unsigned char* row = vt + t * C::ROW + gq * DL * 2;
+            uint4 x[DL / 8];
+#pragma unroll
+            for (int c = 0; c < DL / 8; ++c)
+                x[c] = *reinterpret_cast<const uint4*>(row + 16 * (c ^ vswap));
+#pragma unroll
+            for (int c = 0; c < DL / 8; ++c) {
+                const uint4 v = (DL / 8 == 2) ? sel4(vswap != 0, x[(c ^ 1) & (DL / 8 - 1)], x[c]) : x[c];
+                vw[i][4 * c] = v.x; vw[i][4 * c + 1] = v.y;
+                vw[i][4 * c + 2] = v.z; vw[i][4 * c + 3] = v.w;
             }
         }
     };
@@ -460,7 +472,23 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
             first_j = mt.z;
             plen = mt.w;
             const unsigned char* qs = region + C::OFF_Q + s * C::QBYTES;
-            if constexpr (kMma) {
+            if constexpr (k16) {
+                // q^T as the B operand, with the contraction index permuted so
+                // that one 16-byte load of a K row serves two k-steps: k-steps
+                // 2c and 2c + 1 of lane tq read dims 32c + 8tq + [0, 4) and
+                // 32c + 8tq + [4, 8) (the same permutation for K below)
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint4 y = make_uint4(0u, 0u, 0u, 0u);
+                    if (gq < G) y = *reinterpret_cast<const uint4*>(qs + 2 * (gq * D + 32 * c + 8 * tq));
+                    qb[2 * c][0] = y.x; qb[2 * c][1] = y.y;
+                    qb[2 * c + 1][0] = y.z; qb[2 * c + 1][1] = y.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) { m[e] = -INFINITY; lsum[e] = 0.f; }
+#pragma unroll
+                for (int i = 0; i < MT; ++i) oa[i][0] = oa[i][1] = oa[i][2] = oa[i][3] = 0.f;
+            } else {
                 // lane's dims for k-step kk: 16*tq + 4*(kk%4) + 64*(kk/4) + {0..3}
                 // (a fixed permutation of the contraction index, shared with K)
 #pragma unroll
@@ -477,29 +505,26 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                         qb[kk][1] = *reinterpret_cast<const uint32_t*>(&h1v);
                     }
                 }
-            } else {
 #pragma unroll
-                for (int h = 0; h < G; ++h)
+                for (int h = 0; h < G; ++h) {
+                    m[h] = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < C::NV; ++c)
-                        load_q_pairs<QT, C::EV / 2>(qs, h * D + c * 8 * C::EV + r8 * C::EV,
-                                                    p.qscale, &q2[h][c * C::EV / 2]);
+                    for (int i = 0; i < C::DPL / 2; ++i) o2[h][i] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int x = 0; x < 2; ++x) lsum[x] = 0.f;
             }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                m[h] = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < C::DPL / 2; ++i) o2[h][i] = make_float2(0.f, 0.f);
-            }
-#pragma unroll
-            for (int x = 0; x < LS; ++x) lsum[x] = 0.f;
         }
         last_j = mt.z;
 
         if (flags & 1) {
             const unsigned char* kt = region + s * C::STAGE;
             const unsigned char* vt = kt + C::TILE;
-            if constexpr (!C::kI8) {
+            const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
+            float ksc = 1.f, vsc = 1.f;
+            // scores S[token][head]: two accumulator chains (even / odd k-steps)
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            if constexpr (k16) {
                 if (flags & 4) {   // fused step: the new token's row goes to the cache
                     const int r = (mt.w - 1) % kBlockSize;
                     const long long tile = (long long)__float_as_int(scl[s].x) * p.hkv + (mt.y & 0xffff);
@@ -513,19 +538,36 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                         vd[wv] = vs[wv];
                     }
                 }
-            }
-            const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
-            float ksc = 1.f, vsc = 1.f;
-            if constexpr (C::kI8) {
+                // Rows are 256 B apart, so all rows share the bank mapping: lanes
+                // of odd gq read the two k-step pairs of a 128-byte half in the
+                // other order, which spreads each quarter warp over all 32 banks,
+                // and the pairs are put back in order in registers.
+                const bool kswap = (gq & 1) != 0;
+#pragma unroll
+                for (int c2 = 0; c2 < D / 32; c2 += 2) {
+                    uint4 y[2][2];   // [load h: pair c2 + (h ^ kswap)][row gq, gq + 8]
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int off = 64 * (c2 + (h ^ (kswap ? 1 : 0))) + 16 * tq;
+                        y[h][0] = *reinterpret_cast<const uint4*>(kt + gq * C::ROW + off);
+                        y[h][1] = *reinterpret_cast<const uint4*>(kt + (gq + 8) * C::ROW + off);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = c2 + h;
+                        const uint4 x0 = sel4(kswap, y[h ^ 1][0], y[h][0]);
+                        const uint4 x1 = sel4(kswap, y[h ^ 1][1], y[h][1]);
+                        const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y};
+                        const uint32_t a1[4] = {x0.z, x1.z, x0.w, x1.w};
+                        mma16816<KV>(acc[0], a0, qb[2 * c][0], qb[2 * c][1]);
+                        mma16816<KV>(acc[1], a1, qb[2 * c + 1][0], qb[2 * c + 1][1]);
+                    }
+                }
+            } else {
                 const float2 sc = scl[s];
                 ksc = sc.x;
                 vsc = sc.y;
-            }
-            float alpha[G];
-            if constexpr (kMma) {
-                // scores on the tensor cores: rows gq, gq + 8 of the tile, the
-                // lane's 16-byte chunk of each half row holds 4 k-steps' columns
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // the lane's 16-byte chunk of each half row holds 4 k-steps' columns
                 uint32_t w0[D / 16], w1[D / 16];
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
@@ -541,22 +583,86 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                                   i8x2_to_h2(u0, 0x4342), i8x2_to_h2(u1, 0x4342),
                                   qb[kk][0], qb[kk][1]);
                 }
-                const float sk = p.qscale * ksc;
-                float sv[2][2];   // [token gq / gq + 8][head 2tq + e]
+            }
+            const float sk = p.qscale * ksc;
+            float sv[2][2];   // [token gq / gq + 8][head 2tq + e]
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const bool hv = 2 * tq + e < G;
+                sv[0][e] = (hv && gq < nv) ? (acc[0][e] + acc[1][e]) * sk : -INFINITY;
+                sv[1][e] = (hv && gq + 8 < nv) ? (acc[0][2 + e] + acc[1][2 + e]) * sk : -INFINITY;
+            }
+            float bme[2];    // block max of heads 2tq + e over the 16 tokens
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                bme[e] = fmaxf(sv[0][e], sv[1][e]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1)
+                    bme[e] = fmaxf(bme[e], __shfl_xor_sync(kFull, bme[e], off));
+            }
+            if constexpr (k16) {
+                float alpha[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool hv = 2 * tq + e < G;
-                    sv[0][e] = (hv && gq < nv) ? (acc[0][e] + acc[1][e]) * sk : -INFINITY;
-                    sv[1][e] = (hv && gq + 8 < nv) ? (acc[0][2 + e] + acc[1][2 + e]) * sk : -INFINITY;
+                    const float mn = fmaxf(m[e], bme[e]);
+                    alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m[e] - mn);
+                    m[e] = mn;
+                    const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mn);
+                    const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mn);
+                    lsum[e] = lsum[e] * alpha[e] + p0 + p1;
+                    if (2 * tq + e < G) {   // P[head][token]
+                        pbuf[(2 * tq + e) * kBlockSize + gq] = p0;
+                        pbuf[(2 * tq + e) * kBlockSize + gq + 8] = p1;
+                    }
                 }
-                float bme[2];
+                if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    bme[e] = fmaxf(sv[0][e], sv[1][e]);
-#pragma unroll
-                    for (int off = 4; off < 32; off <<= 1)
-                        bme[e] = fmaxf(bme[e], __shfl_xor_sync(kFull, bme[e], off));
+                    for (int i = 0; i < MT; ++i) {
+                        oa[i][0] *= alpha[0]; oa[i][1] *= alpha[1];
+                        oa[i][2] *= alpha[0]; oa[i][3] *= alpha[1];
+                    }
                 }
+                load_v(vt);
+                // V rows past the context are zeroed (they may hold anything,
+                // and 0 * NaN would poison the sum)
+                if (nv < kBlockSize) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (2 * tq + (i & 1) + 8 * (i >> 1) >= nv)
+#pragma unroll
+                            for (int c = 0; c < DL / 2; ++c) vw[i][c] = 0u;
+                }
+                __syncwarp();
+                // P^T as the B operand: column gq = head gq, tokens 2tq, 2tq + 1 | + 8.
+                // P = hi + lo in two 16-bit parts (hi = rn(P), lo = rn(P - hi), the
+                // difference exact in fp32), so the weights keep ~2^-18 relative
+                // precision: with a 16-bit P alone a two-token context would be off
+                // by up to 2^-9 |v|.
+                uint32_t ph[2] = {0u, 0u}, pl[2] = {0u, 0u};
+                if (gq < G) {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 f = *reinterpret_cast<const float2*>(pbuf + gq * kBlockSize + 2 * tq + 8 * k);
+                        ph[k] = pack2<KV>(f.x, f.y);
+                        const float2 r = unpack2(KV{}, ph[k]);
+                        pl[k] = pack2<KV>(f.x - r.x, f.y - r.y);
+                    }
+                }
+                // V^T A fragments: m-tile i rows gq, gq + 8 = dims gq*DL + 2i, + 1
+                uint32_t va[MT][4];
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    va[i][0] = __byte_perm(vw[0][i], vw[1][i], 0x5410);
+                    va[i][1] = __byte_perm(vw[0][i], vw[1][i], 0x7632);
+                    va[i][2] = __byte_perm(vw[2][i], vw[3][i], 0x5410);
+                    va[i][3] = __byte_perm(vw[2][i], vw[3][i], 0x7632);
+                }
+#pragma unroll
+                for (int i = 0; i < MT; ++i) mma16816<KV>(oa[i], va[i], ph[0], ph[1]);
+#pragma unroll
+                for (int i = 0; i < MT; ++i) mma16816<KV>(oa[i], va[i], pl[0], pl[1]);
+            } else {
+                float alpha[G];
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     const float bmh = __shfl_sync(kFull, bme[hh & 1], hh >> 1);
@@ -578,94 +684,40 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodePara
                         pbuf[(gq + 8) * G + 2 * tq + e] = p1 * vsc;
                     }
                 }
-            } else {
-                // scores: acc[k*G + h] = <q_h, K[rgrp + 4k]> over the lane's dims
-                float acc[C::NVAL];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const unsigned char* row = kt + (rgrp + 4 * k) * C::ROW;
-                    float2 kf[C::E / 2];
+                for (int h = 0; h < G; ++h)
 #pragma unroll
-                    for (int c = 0; c < C::NV; ++c)
-                        load_pairs_smem<KV, C::VB>(row + c * 8 * C::VB + r8 * C::VB,
-                                                   &kf[c * C::EV / 2]);
+                    for (int i = 0; i < C::DPL / 2; ++i)
+                        o2[h][i] = make_float2(o2[h][i].x * alpha[h], o2[h][i].y * alpha[h]);
+                __syncwarp();
+                // P.V over the valid rows of the tile
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float2 a = make_float2(0.f, 0.f);
+                for (int t = 0; t < kBlockSize; ++t) {
+                    if (t < nv) {
+                        float pv[G];
+                        if constexpr (G == 4) {
+                            const float4 x = *reinterpret_cast<const float4*>(pbuf + t * 4);
+                            pv[0] = x.x; pv[1] = x.y; pv[2] = x.z; pv[3] = x.w;
+                        } else if constexpr (G == 2) {
+                            const float2 x = *reinterpret_cast<const float2*>(pbuf + t * 2);
+                            pv[0] = x.x; pv[1] = x.y;
+                        } else {
+                            pv[0] = pbuf[t];
+                        }
+                        float2 vf[C::DPL / 2];
+                        load_pairs_smem<KV, C::DPL * C::esize>(vt + t * C::ROW + lane * C::DPL * C::esize,
+                                                              vf);
 #pragma unroll
-                        for (int i = 0; i < C::E / 2; ++i) a = __ffma2_rn(q2[h][i], kf[i], a);
-                        acc[k * G + h] = a.x + a.y;
+                        for (int h = 0; h < G; ++h)
+#pragma unroll
+                            for (int i = 0; i < C::DPL / 2; ++i)
+                                o2[h][i] = __ffma2_rn(make_float2(pv[h], pv[h]), vf[i], o2[h][i]);
                     }
-                }
-                int xb = 0;
-                xstep<C::NVAL>(acc, 4, lane, xb);
-                xstep<(C::NVAL >= 2 ? C::NVAL / 2 : 1)>(acc, 2, lane, xb);
-                xstep<(C::NVAL >= 4 ? C::NVAL / 4 : 1)>(acc, 1, lane, xb);
-                float sc[C::NF];
-#pragma unroll
-                for (int x = 0; x < C::NF; ++x) sc[x] = (my_t < nv) ? acc[x] * ksc : -INFINITY;
-                // per-head block max, new running max, rescale factors
-                float bm[G];
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    bm[hh] = (hh / C::NF == h0 / C::NF) ? sc[hh % C::NF] : -INFINITY;
-#pragma unroll
-                for (int off = 16; off; off >>= 1)
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-                        bm[hh] = fmaxf(bm[hh], __shfl_xor_sync(kFull, bm[hh], off));
-    #pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float mn = fmaxf(m[hh], bm[hh]);
-                    alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m[hh] - mn);
-                    m[hh] = mn;
-                }
-                float pr[C::NF];
-#pragma unroll
-                for (int x = 0; x < C::NF; ++x) {
-                    float mh = m[x], ah = alpha[x];
-#pragma unroll
-                    for (int cand = 1; cand < G / C::NF; ++cand)
-                        if (h0 == cand * C::NF) { mh = m[cand * C::NF + x]; ah = alpha[cand * C::NF + x]; }
-                    pr[x] = (sc[x] == -INFINITY) ? 0.f : fast_exp2(sc[x] - mh);
-                    lsum[x] = lsum[x] * ah + pr[x];
-                }
-                if (!dup) {
-#pragma unroll
-                    for (int x = 0; x < C::NF; ++x) pbuf[my_t * G + h0 + x] = pr[x] * vsc;
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int i = 0; i < C::DPL / 2; ++i)
-                    o2[h][i] = make_float2(o2[h][i].x * alpha[h], o2[h][i].y * alpha[h]);
-            __syncwarp();
-            // P.V over the valid rows of the tile
-#pragma unroll
-            for (int t = 0; t < kBlockSize; ++t) {
-                if (t < nv) {
-                    float pv[G];
-                    if constexpr (G == 4) {
-                        const float4 x = *reinterpret_cast<const float4*>(pbuf + t * 4);
-                        pv[0] = x.x; pv[1] = x.y; pv[2] = x.z; pv[3] = x.w;
-                    } else if constexpr (G == 2) {
-                        const float2 x = *reinterpret_cast<const float2*>(pbuf + t * 2);
-                        pv[0] = x.x; pv[1] = x.y;
-                    } else {
-                        pv[0] = pbuf[t];
-                    }
-                    float2 vf[C::DPL / 2];
-                    load_pairs_smem<KV, C::DPL * C::esize>(vt + t * C::ROW + lane * C::DPL * C::esize,
-                                                          vf);
-#pragma unroll
-                    for (int h = 0; h < G; ++h)
-#pragma unroll
-                        for (int i = 0; i < C::DPL / 2; ++i)
-                            o2[h][i] = __ffma2_rn(make_float2(pv[h], pv[h]), vf[i], o2[h][i]);
                 }
             }
         }
+        // The stage goes back to the copy engine only after the math: releasing
+        // it right after its reads (with V held in registers) measured slower.
         __syncwarp();
         if (u_issue < u1) {
             issue(u_issue, s);
@@ -729,7 +781,6 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
     __shared__ float s_m[kCombineThreads], s_den[kCombineThreads];
     __shared__ float4 s_num[kCombineThreads];
     griddep_wait();                 // partials come from the split grid
-    griddep_launch_dependents();
     const int seg = blockIdx.x;
     const int b = seg / c.hkv, kvh = seg - b * c.hkv;
     const int* P = c.ws_prefix;
@@ -774,6 +825,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
     const float inv = den > 0.f ? 1.0f / den : 0.f;
     const float2 v[2] = {make_float2(num.x, num.y), make_float2(num.z, num.w)};
     store_out<QT, 4>(c.out, obase, v, inv);
+    // Only now may the next grid start launching: a decode split launched
+    // early here would take SM resources while this grid still runs, which
+    // measured ~30 % slower steps.
+    griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------- host ---
