@@ -60,8 +60,6 @@ struct Cfg {
     // that 3 CTAs of 4 warps share an SM (at least 2 stages).
     static constexpr int QBYTES = G * D * 2;   // q rows of one (sequence, kv head)
     static constexpr int NS = (19456 / (STAGE + QBYTES)) < 2 ? 2 : (19456 / (STAGE + QBYTES));
-    // INT8 P.V on the CUDA cores: each lane owns D/32 output dims.
-    static constexpr int DPL = D / 32;
     // Per-warp shared-memory region.
     static constexpr int OFF_BAR = NS * STAGE;                       // 8-byte mbarriers
     static constexpr int OFF_META = align_up(OFF_BAR + NS * 8, 16);   // int4 per stage
@@ -160,44 +158,6 @@ __device__ __forceinline__ void decode_unit(long long u, const int* prefix, int 
     const int r = int(u - (long long)hkv * prefix[b]);
     kvh = r / nb;
     j = r - kvh * nb;
-}
-
-// Raw words of one vector load from shared memory -> float2 pairs.
-template <typename KV, int VB>
-__device__ __forceinline__ void load_pairs_smem(const unsigned char* src, float2* dst) {
-    uint32_t w[VB / 4 > 0 ? VB / 4 : 1];
-    if constexpr (VB == 16) {
-        const uint4 x = *reinterpret_cast<const uint4*>(src);
-        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-    } else if constexpr (VB == 8) {
-        const uint2 x = *reinterpret_cast<const uint2*>(src);
-        w[0] = x.x; w[1] = x.y;
-    } else if constexpr (VB == 4) {
-        w[0] = *reinterpret_cast<const uint32_t*>(src);
-    } else {  // 2 bytes: two int8 codes
-        w[0] = *reinterpret_cast<const uint16_t*>(src);
-    }
-    if constexpr (Elem<KV>::bytes == 2) {
-#pragma unroll
-        for (int i = 0; i < VB / 4; ++i) dst[i] = unpack2(KV{}, w[i]);
-    } else {
-        // int8 codes -> floats: biased byte as the low mantissa byte of 2^23,
-        // then one packed subtraction of 2^23 + 128 per pair (exact)
-        constexpr int NW = VB >= 4 ? VB / 4 : 1;
-        const float2 bias = make_float2(-8388736.0f, -8388736.0f);
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            const uint32_t u = w[i] ^ 0x80808080u;
-            dst[2 * i] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                                                __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
-                                    bias);
-            if (VB >= 4)
-                dst[2 * i + 1] = __fadd2_rn(
-                    make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                                __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
-                    bias);
-        }
-    }
 }
 
 template <typename QT, int DPL>
@@ -333,116 +293,131 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
         }
     };
 
-    // ---- consumer: both paths score on the tensor cores (mma.sync m16n8k16,
-    // fp32 accumulators) with rows = the tile's 16 tokens and columns = the g
-    // heads (padded to 8). Lane (gq, tq) = (lane / 4, lane % 4) then holds
-    // tokens gq and gq + 8 of heads 2tq and 2tq + 1.
-    //  * 16-bit caches: P.V also runs on the tensor cores as
-    //    O^T[dims x heads] += V^T[dims x 16 tokens] P^T[16 tokens x heads]; lane
+    // ---- consumer: scores and P.V on the tensor cores (mma.sync m16n8k16,
+    // fp32 accumulators), all cache types alike:
+    //  * S[16 tokens x heads]: rows = the tile's tokens, columns = the g heads
+    //    (padded to 8). Lane (gq, tq) = (lane / 4, lane % 4) then holds tokens
+    //    gq and gq + 8 of heads 2tq and 2tq + 1.
+    //  * O^T[dims x heads] += V^T[dims x 16 tokens] P^T[16 tokens x heads]: lane
     //    (gq, tq) accumulates dims [gq*D/8, (gq+1)*D/8) of heads 2tq, 2tq + 1,
     //    so its softmax state is that of its own two heads.
-    //  * INT8 caches: K codes become fp16 exactly for the scores; P.V on the
-    //    CUDA cores, each lane owning D/32 output dims of every head.
-    constexpr bool k16 = !C::kI8;
-    constexpr int MT = D / 16;                   // m-tiles of P.V (16-bit path)
+    // 16-bit caches multiply in their own type; INT8 codes become fp16 exactly
+    // (the biased byte as the low mantissa byte of 1024, then one packed
+    // subtraction), q is rounded to fp16 and the block's V scale rides on P.
+    using MMT = typename std::conditional<C::kI8, F16, KV>::type;   // mma operand type
+    constexpr int MT = D / 16;                   // m-tiles of P.V
     constexpr int DL = D / 8;                    // dims a lane row group owns
     const int gq = lane >> 2, tq = lane & 3;
     uint32_t qb[D / 16][2];                      // B fragments of q, per k-step
-    float m[k16 ? 2 : G], lsum[2] = {0.f, 0.f};
-    float oa[k16 ? MT : 1][4];                   // 16-bit: O^T accumulators
-    float2 o2[k16 ? 1 : G][k16 ? 1 : C::DPL / 2];  // INT8: per-head output dims
+    float m[2], lsum[2] = {0.f, 0.f};            // heads 2tq, 2tq + 1
+    float oa[MT][4];                             // O^T accumulators
     int pb = -1, pkvh = -1, first_j = 0, last_j = 0, plen = 0;
-
-    // Does this lane's lsum hold a partial of head hh (INT8 path), and where?
-    auto owns = [&](int hh) -> bool { return (hh >> 1) == tq; };
-    auto lidx = [&](int hh) -> int { return hh & 1; };
+    // INT8: P carries the block's V scale into fp16, so O is kept in units of
+    // 2^vexp (vexp >= 0, raised when a scale would push P past 2^14, i.e.
+    // toward the fp16 limit) and multiplied back when the piece is written.
+    int vexp = 0;
+    float vmul = 1.f;                            // 2^-vexp
 
     auto finalize = [&]() {
         const int nbk = prefix[pb + 1] - prefix[pb];
         const long long seg = (long long)pb * p.hkv + pkvh;
         const bool whole = (first_j == 0 && last_j == nbk - 1);
-        if constexpr (k16) {
-            float lh[2] = {lsum[0], lsum[1]};
+        float lh[2] = {lsum[0], lsum[1]};
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1)
+        for (int off = 4; off < 32; off <<= 1)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) lh[e] += __shfl_xor_sync(kFull, lh[e], off);
+            for (int e = 0; e < 2; ++e) lh[e] += __shfl_xor_sync(kFull, lh[e], off);
+        const float up = C::kI8 ? ldexpf(1.f, vexp) : 1.f;   // O back from units of 2^vexp
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int h = 2 * tq + e;
-                if (h >= G) continue;
-                if (whole) {
-                    float2 v[MT];
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) v[mt] = make_float2(oa[mt][e], oa[mt][2 + e]);
-                    const float inv = lh[e] > 0.f ? 1.0f / lh[e] : 0.f;
-                    store_out<QT, DL>(p.out, ((long long)pb * p.hq + pkvh * G + h) * D + gq * DL, v,
-                                      inv);
-                } else {
-                    const long long slot = seg + w;
-                    float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * G + h) * D + gq * DL);
-#pragma unroll
-                    for (int i = 0; i < MT / 2; ++i)
-                        dst[i] = make_float4(oa[2 * i][e], oa[2 * i][2 + e], oa[2 * i + 1][e],
-                                             oa[2 * i + 1][2 + e]);
-                    if (gq == 0)
-                        *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) =
-                            make_float2(m[e], lh[e]);
-                }
-            }
-        } else {
-            float lh[G];
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) lh[hh] = owns(hh) ? lsum[lidx(hh)] : 0.f;
-#pragma unroll
-            for (int off = 16; off; off >>= 1)
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) lh[hh] += __shfl_xor_sync(kFull, lh[hh], off);
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * tq + e;
+            if (h >= G) continue;
             if (whole) {
+                float2 v[MT];
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
-                    const long long off = ((long long)pb * p.hq + pkvh * G + h) * D + lane * C::DPL;
-                    store_out<QT, C::DPL>(p.out, off, o2[h], inv);
-                }
+                for (int i = 0; i < MT; ++i) v[i] = make_float2(oa[i][e], oa[i][2 + e]);
+                const float inv = lh[e] > 0.f ? up / lh[e] : 0.f;
+                store_out<QT, DL>(p.out, ((long long)pb * p.hq + pkvh * G + h) * D + gq * DL, v, inv);
             } else {
                 const long long slot = seg + w;
+                float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * G + h) * D + gq * DL);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float* dst = p.part_o + ((slot * G + h) * D + lane * C::DPL);
-                    if constexpr (C::DPL == 4)
-                        *reinterpret_cast<float4*>(dst) =
-                            make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
-                    else
-                        *reinterpret_cast<float2*>(dst) = o2[h][0];
-                    if (lane == 0)
-                        *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) =
-                            make_float2(m[h], lh[h]);
-                }
+                for (int i = 0; i < MT / 2; ++i)
+                    dst[i] = make_float4(oa[2 * i][e] * up, oa[2 * i][2 + e] * up,
+                                         oa[2 * i + 1][e] * up, oa[2 * i + 1][2 + e] * up);
+                if (gq == 0)
+                    *reinterpret_cast<float2*>(p.part_ml + (slot * G + h) * 2) = make_float2(m[e], lh[e]);
             }
         }
     };
 
-    uint32_t vw[k16 ? 4 : 1][k16 ? DL / 2 : 1];   // V fragments of the current unit
-    // V fragments of the unit in stage s: rows 2tq, 2tq + 1, 2tq + 8, 2tq + 9,
-    // the lane row group's DL dims (16-bit path)
-    auto load_v = [&](const unsigned char* vt) {
-        // V: lanes of odd tq read a row's two 16-byte chunks in the
-        // other order (halves the bank conflicts of the four rows)
-        const int vswap = (DL / 8 == 2) ? (tq & 1) : 0;
+    // A fragments of V^T for m-tile i: rows gq, gq + 8 = dims gq*DL + 2i, + 1;
+    // columns = tokens 2tq, 2tq + 1 (a0, a1) and 2tq + 8, 2tq + 9 (a2, a3).
+    // Tokens at or past `nv` are zeroed (stale rows may hold anything, and
+    // 0 * NaN would poison the sum).
+    uint32_t va[MT][4];
+    auto load_v = [&](const unsigned char* vt, int nv) {
+        if constexpr (!C::kI8) {
+            // 16-bit: a lane reads DL dims of each of its four rows; lanes of
+            // odd tq read a row's two 16-byte chunks in the other order (halves
+            // the bank conflicts of rows that share the bank mapping)
+            uint32_t vw[4][DL / 2];
+            const int vswap = (DL / 8 == 2) ? (tq & 1) : 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
-            const unsigned char* row = vt + t * C::ROW + gq * DL * 2;
-            uint4 x[DL / 8];
+            for (int i = 0; i < 4; ++i) {
+                const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
+                const unsigned char* row = vt + t * C::ROW + gq * DL * 2;
+                uint4 x[DL / 8];
 #pragma unroll
-            for (int c = 0; c < DL / 8; ++c)
-                x[c] = *reinterpret_cast<const uint4*>(row + 16 * (c ^ vswap));
+                for (int c = 0; c < DL / 8; ++c)
+                    x[c] = *reinterpret_cast<const uint4*>(row + 16 * (c ^ vswap));
+                const bool keep = t < nv;
 #pragma unroll
-            for (int c = 0; c < DL / 8; ++c) {
-                const uint4 v = (DL / 8 == 2) ? sel4(vswap != 0, x[(c ^ 1) & (DL / 8 - 1)], x[c]) : x[c];
-                vw[i][4 * c] = v.x; vw[i][4 * c + 1] = v.y;
-                vw[i][4 * c + 2] = v.z; vw[i][4 * c + 3] = v.w;
+                for (int c = 0; c < DL / 8; ++c) {
+                    uint4 v = (DL / 8 == 2) ? sel4(vswap != 0, x[(c ^ 1) & (DL / 8 - 1)], x[c]) : x[c];
+                    if (!keep) v = make_uint4(0u, 0u, 0u, 0u);
+                    vw[i][4 * c] = v.x; vw[i][4 * c + 1] = v.y;
+                    vw[i][4 * c + 2] = v.z; vw[i][4 * c + 3] = v.w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                va[i][0] = __byte_perm(vw[0][i], vw[1][i], 0x5410);
+                va[i][1] = __byte_perm(vw[0][i], vw[1][i], 0x7632);
+                va[i][2] = __byte_perm(vw[2][i], vw[3][i], 0x5410);
+                va[i][3] = __byte_perm(vw[2][i], vw[3][i], 0x7632);
+            }
+        } else {
+            // INT8: DL codes per row; the bytes of two tokens are interleaved,
+            // then each pair becomes fp16x2 exactly
+            uint32_t vw[4][DL / 4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
+                const unsigned char* row = vt + t * C::ROW + gq * DL;
+                const bool keep = t < nv;
+                if constexpr (DL == 16) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(row);
+                    vw[i][0] = keep ? x.x : 0u; vw[i][1] = keep ? x.y : 0u;
+                    vw[i][2] = keep ? x.z : 0u; vw[i][3] = keep ? x.w : 0u;
+                } else {
+                    const uint2 x = *reinterpret_cast<const uint2*>(row);
+                    vw[i][0] = keep ? x.x : 0u; vw[i][1] = keep ? x.y : 0u;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < DL / 4; ++k) {
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {   // bytes 0-1 -> m-tile 2k, bytes 2-3 -> 2k + 1
+                    const uint32_t sel = hb ? 0x7362u : 0x5140u;
+                    const uint32_t x = __byte_perm(vw[0][k], vw[1][k], sel) ^ 0x80808080u;
+                    const uint32_t y = __byte_perm(vw[2][k], vw[3][k], sel) ^ 0x80808080u;
+                    const int i = 2 * k + hb;
+                    va[i][0] = i8x2_to_h2(x, 0x4140);
+                    va[i][1] = i8x2_to_h2(x, 0x4342);
+                    va[i][2] = i8x2_to_h2(y, 0x4140);
+                    va[i][3] = i8x2_to_h2(y, 0x4342);
+                }
             }
         }
     };
@@ -472,48 +447,38 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
             first_j = mt.z;
             plen = mt.w;
             const unsigned char* qs = region + C::OFF_Q + s * C::QBYTES;
-            if constexpr (k16) {
-                // q^T as the B operand, with the contraction index permuted so
-                // that one 16-byte load of a K row serves two k-steps: k-steps
-                // 2c and 2c + 1 of lane tq read dims 32c + 8tq + [0, 4) and
-                // 32c + 8tq + [4, 8) (the same permutation for K below)
+            // q^T as the B operand, with the contraction index permuted so that
+            // one 16-byte load of a K row serves several k-steps. 16-bit: k-steps
+            // 2c and 2c + 1 of lane tq read dims 32c + 8tq + [0, 4) and + [4, 8).
+            // INT8: k-step kk of lane tq reads dims 16tq + 4(kk%4) + 64(kk/4) + [0, 4).
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
+                if constexpr (!C::kI8) {
                     uint4 y = make_uint4(0u, 0u, 0u, 0u);
                     if (gq < G) y = *reinterpret_cast<const uint4*>(qs + 2 * (gq * D + 32 * c + 8 * tq));
                     qb[2 * c][0] = y.x; qb[2 * c][1] = y.y;
                     qb[2 * c + 1][0] = y.z; qb[2 * c + 1][1] = y.w;
-                }
+                } else {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) { m[e] = -INFINITY; lsum[e] = 0.f; }
-#pragma unroll
-                for (int i = 0; i < MT; ++i) oa[i][0] = oa[i][1] = oa[i][2] = oa[i][3] = 0.f;
-            } else {
-                // lane's dims for k-step kk: 16*tq + 4*(kk%4) + 64*(kk/4) + {0..3}
-                // (a fixed permutation of the contraction index, shared with K)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    qb[kk][0] = qb[kk][1] = 0u;
-                    if (gq < G) {
-                        const int d0 = 16 * tq + 4 * (kk % 4) + 64 * (kk / 4);
-                        const uint2 x = *reinterpret_cast<const uint2*>(
-                            qs + 2 * (gq * D + d0));
-                        const float2 f0 = unpack2(QT{}, x.x), f1 = unpack2(QT{}, x.y);
-                        const __half2 h0v = __floats2half2_rn(f0.x, f0.y);
-                        const __half2 h1v = __floats2half2_rn(f1.x, f1.y);
-                        qb[kk][0] = *reinterpret_cast<const uint32_t*>(&h0v);
-                        qb[kk][1] = *reinterpret_cast<const uint32_t*>(&h1v);
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * c + h;
+                        qb[kk][0] = qb[kk][1] = 0u;
+                        if (gq < G) {
+                            const int d0 = 16 * tq + 4 * (kk % 4) + 64 * (kk / 4);
+                            const uint2 x = *reinterpret_cast<const uint2*>(qs + 2 * (gq * D + d0));
+                            const float2 f0 = unpack2(QT{}, x.x), f1 = unpack2(QT{}, x.y);
+                            qb[kk][0] = pack2<F16>(f0.x, f0.y);
+                            qb[kk][1] = pack2<F16>(f1.x, f1.y);
+                        }
                     }
                 }
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    m[h] = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < C::DPL / 2; ++i) o2[h][i] = make_float2(0.f, 0.f);
-                }
-#pragma unroll
-                for (int x = 0; x < 2; ++x) lsum[x] = 0.f;
             }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) { m[e] = -INFINITY; lsum[e] = 0.f; }
+#pragma unroll
+            for (int i = 0; i < MT; ++i) oa[i][0] = oa[i][1] = oa[i][2] = oa[i][3] = 0.f;
+            vexp = 0;
+            vmul = 1.f;
         }
         last_j = mt.z;
 
@@ -522,9 +487,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
             const unsigned char* vt = kt + C::TILE;
             const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
             float ksc = 1.f, vsc = 1.f;
-            // scores S[token][head]: two accumulator chains (even / odd k-steps)
+            // scores S[token][head]: two accumulator chains (even / odd k-steps).
+            // Rows are D * esize bytes apart, a multiple of 128, so all rows
+            // share the bank mapping: lanes of odd gq read the two k-step groups
+            // of a 128-byte span in the other order, which spreads each quarter
+            // warp over all 32 banks, and the groups are put back in registers.
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            if constexpr (k16) {
+            const bool kswap = (gq & 1) != 0;
+            if constexpr (!C::kI8) {
                 if (flags & 4) {   // fused step: the new token's row goes to the cache
                     const int r = (mt.w - 1) % kBlockSize;
                     const long long tile = (long long)__float_as_int(scl[s].x) * p.hkv + (mt.y & 0xffff);
@@ -538,11 +508,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                         vd[wv] = vs[wv];
                     }
                 }
-                // Rows are 256 B apart, so all rows share the bank mapping: lanes
-                // of odd gq read the two k-step pairs of a 128-byte half in the
-                // other order, which spreads each quarter warp over all 32 banks,
-                // and the pairs are put back in order in registers.
-                const bool kswap = (gq & 1) != 0;
 #pragma unroll
                 for (int c2 = 0; c2 < D / 32; c2 += 2) {
                     uint4 y[2][2];   // [load h: pair c2 + (h ^ kswap)][row gq, gq + 8]
@@ -567,12 +532,33 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                 const float2 sc = scl[s];
                 ksc = sc.x;
                 vsc = sc.y;
+                if (vsc * vmul >= 16384.f) {   // warp-uniform; raise vexp, rescale O exactly
+                    int ex;
+                    frexpf(vsc, &ex);           // vsc < 2^ex
+                    const int nexp = ex - 14;   // vsc * 2^-nexp < 2^14
+                    const float r = ldexpf(1.f, vexp - nexp);
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        oa[i][0] *= r; oa[i][1] *= r; oa[i][2] *= r; oa[i][3] *= r;
+                    }
+                    vexp = nexp;
+                    vmul = ldexpf(1.f, -nexp);
+                }
+                vsc *= vmul;
                 // the lane's 16-byte chunk of each half row holds 4 k-steps' columns
+                constexpr int NC = D / 64;
+                uint4 y[NC][2];
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int cc = (NC == 2) ? (c ^ (kswap ? 1 : 0)) : c;
+                    y[c][0] = *reinterpret_cast<const uint4*>(kt + gq * C::ROW + 64 * cc + 16 * tq);
+                    y[c][1] = *reinterpret_cast<const uint4*>(kt + (gq + 8) * C::ROW + 64 * cc + 16 * tq);
+                }
                 uint32_t w0[D / 16], w1[D / 16];
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    const uint4 x0 = *reinterpret_cast<const uint4*>(kt + gq * C::ROW + 64 * c + 16 * tq);
-                    const uint4 x1 = *reinterpret_cast<const uint4*>(kt + (gq + 8) * C::ROW + 64 * c + 16 * tq);
+                for (int c = 0; c < NC; ++c) {
+                    const uint4 x0 = (NC == 2) ? sel4(kswap, y[(c ^ 1) & (NC - 1)][0], y[c][0]) : y[c][0];
+                    const uint4 x1 = (NC == 2) ? sel4(kswap, y[(c ^ 1) & (NC - 1)][1], y[c][1]) : y[c][1];
                     w0[4 * c] = x0.x; w0[4 * c + 1] = x0.y; w0[4 * c + 2] = x0.z; w0[4 * c + 3] = x0.w;
                     w1[4 * c] = x1.x; w1[4 * c + 1] = x1.y; w1[4 * c + 2] = x1.z; w1[4 * c + 3] = x1.w;
                 }
@@ -592,129 +578,51 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                 sv[0][e] = (hv && gq < nv) ? (acc[0][e] + acc[1][e]) * sk : -INFINITY;
                 sv[1][e] = (hv && gq + 8 < nv) ? (acc[0][2 + e] + acc[1][2 + e]) * sk : -INFINITY;
             }
-            float bme[2];    // block max of heads 2tq + e over the 16 tokens
+            float alpha[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                bme[e] = fmaxf(sv[0][e], sv[1][e]);
+                float bme = fmaxf(sv[0][e], sv[1][e]);   // block max over the 16 tokens
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1)
-                    bme[e] = fmaxf(bme[e], __shfl_xor_sync(kFull, bme[e], off));
+                for (int off = 4; off < 32; off <<= 1) bme = fmaxf(bme, __shfl_xor_sync(kFull, bme, off));
+                const float mn = fmaxf(m[e], bme);
+                alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m[e] - mn);
+                m[e] = mn;
+                const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mn);
+                const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mn);
+                lsum[e] = lsum[e] * alpha[e] + p0 + p1;
+                if (2 * tq + e < G) {   // P[head][token], times the block's V scale
+                    pbuf[(2 * tq + e) * kBlockSize + gq] = p0 * vsc;
+                    pbuf[(2 * tq + e) * kBlockSize + gq + 8] = p1 * vsc;
+                }
             }
-            if constexpr (k16) {
-                float alpha[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float mn = fmaxf(m[e], bme[e]);
-                    alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m[e] - mn);
-                    m[e] = mn;
-                    const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mn);
-                    const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mn);
-                    lsum[e] = lsum[e] * alpha[e] + p0 + p1;
-                    if (2 * tq + e < G) {   // P[head][token]
-                        pbuf[(2 * tq + e) * kBlockSize + gq] = p0;
-                        pbuf[(2 * tq + e) * kBlockSize + gq + 8] = p1;
-                    }
-                }
-                if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-                    for (int i = 0; i < MT; ++i) {
-                        oa[i][0] *= alpha[0]; oa[i][1] *= alpha[1];
-                        oa[i][2] *= alpha[0]; oa[i][3] *= alpha[1];
-                    }
-                }
-                load_v(vt);
-                // V rows past the context are zeroed (they may hold anything,
-                // and 0 * NaN would poison the sum)
-                if (nv < kBlockSize) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (2 * tq + (i & 1) + 8 * (i >> 1) >= nv)
-#pragma unroll
-                            for (int c = 0; c < DL / 2; ++c) vw[i][c] = 0u;
-                }
-                __syncwarp();
-                // P^T as the B operand: column gq = head gq, tokens 2tq, 2tq + 1 | + 8.
-                // P = hi + lo in two 16-bit parts (hi = rn(P), lo = rn(P - hi), the
-                // difference exact in fp32), so the weights keep ~2^-18 relative
-                // precision: with a 16-bit P alone a two-token context would be off
-                // by up to 2^-9 |v|.
-                uint32_t ph[2] = {0u, 0u}, pl[2] = {0u, 0u};
-                if (gq < G) {
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const float2 f = *reinterpret_cast<const float2*>(pbuf + gq * kBlockSize + 2 * tq + 8 * k);
-                        ph[k] = pack2<KV>(f.x, f.y);
-                        const float2 r = unpack2(KV{}, ph[k]);
-                        pl[k] = pack2<KV>(f.x - r.x, f.y - r.y);
-                    }
-                }
-                // V^T A fragments: m-tile i rows gq, gq + 8 = dims gq*DL + 2i, + 1
-                uint32_t va[MT][4];
+            if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
-                    va[i][0] = __byte_perm(vw[0][i], vw[1][i], 0x5410);
-                    va[i][1] = __byte_perm(vw[0][i], vw[1][i], 0x7632);
-                    va[i][2] = __byte_perm(vw[2][i], vw[3][i], 0x5410);
-                    va[i][3] = __byte_perm(vw[2][i], vw[3][i], 0x7632);
-                }
-#pragma unroll
-                for (int i = 0; i < MT; ++i) mma16816<KV>(oa[i], va[i], ph[0], ph[1]);
-#pragma unroll
-                for (int i = 0; i < MT; ++i) mma16816<KV>(oa[i], va[i], pl[0], pl[1]);
-            } else {
-                float alpha[G];
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float bmh = __shfl_sync(kFull, bme[hh & 1], hh >> 1);
-                    const float mn = fmaxf(m[hh], bmh);
-                    alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m[hh] - mn);
-                    m[hh] = mn;
-                }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float mh = m[e < G ? e : 0], ah = alpha[e < G ? e : 0];
-#pragma unroll
-                    for (int cand = 1; cand < (G + 1) / 2; ++cand)
-                        if (tq == cand) { mh = m[2 * cand + e]; ah = alpha[2 * cand + e]; }
-                    const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mh);
-                    const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mh);
-                    lsum[e] = lsum[e] * ah + p0 + p1;
-                    if (2 * tq + e < G) {
-                        pbuf[gq * G + 2 * tq + e] = p0 * vsc;
-                        pbuf[(gq + 8) * G + 2 * tq + e] = p1 * vsc;
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int i = 0; i < C::DPL / 2; ++i)
-                        o2[h][i] = make_float2(o2[h][i].x * alpha[h], o2[h][i].y * alpha[h]);
-                __syncwarp();
-                // P.V over the valid rows of the tile
-#pragma unroll
-                for (int t = 0; t < kBlockSize; ++t) {
-                    if (t < nv) {
-                        float pv[G];
-                        if constexpr (G == 4) {
-                            const float4 x = *reinterpret_cast<const float4*>(pbuf + t * 4);
-                            pv[0] = x.x; pv[1] = x.y; pv[2] = x.z; pv[3] = x.w;
-                        } else if constexpr (G == 2) {
-                            const float2 x = *reinterpret_cast<const float2*>(pbuf + t * 2);
-                            pv[0] = x.x; pv[1] = x.y;
-                        } else {
-                            pv[0] = pbuf[t];
-                        }
-                        float2 vf[C::DPL / 2];
-                        load_pairs_smem<KV, C::DPL * C::esize>(vt + t * C::ROW + lane * C::DPL * C::esize,
-                                                              vf);
-#pragma unroll
-                        for (int h = 0; h < G; ++h)
-#pragma unroll
-                            for (int i = 0; i < C::DPL / 2; ++i)
-                                o2[h][i] = __ffma2_rn(make_float2(pv[h], pv[h]), vf[i], o2[h][i]);
-                    }
+                    oa[i][0] *= alpha[0]; oa[i][1] *= alpha[1];
+                    oa[i][2] *= alpha[0]; oa[i][3] *= alpha[1];
                 }
             }
+            load_v(vt, nv);
+            __syncwarp();
+            // P^T as the B operand: column gq = head gq, tokens 2tq, 2tq + 1 | + 8.
+            // P = hi + lo in two parts of the operand type (hi = rn(P), lo =
+            // rn(P - hi), the difference exact in fp32), so the weights keep
+            // ~2^-18 relative precision: with one 16-bit P a two-token context
+            // would be off by up to 2^-9 |v|.
+            uint32_t ph[2] = {0u, 0u}, pl[2] = {0u, 0u};
+            if (gq < G) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float2 f = *reinterpret_cast<const float2*>(pbuf + gq * kBlockSize + 2 * tq + 8 * k);
+                    ph[k] = pack2<MMT>(f.x, f.y);
+                    const float2 r = unpack2(MMT{}, ph[k]);
+                    pl[k] = pack2<MMT>(f.x - r.x, f.y - r.y);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < MT; ++i) mma16816<MMT>(oa[i], va[i], ph[0], ph[1]);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) mma16816<MMT>(oa[i], va[i], pl[0], pl[1]);
         }
         // The stage goes back to the copy engine only after the math: releasing
         // it right after its reads (with V held in registers) measured slower.

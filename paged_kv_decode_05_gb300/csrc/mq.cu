@@ -429,8 +429,17 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 }
             l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
             l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-            const uint32_t pa[4] = {pack2<KV>(pr[0][0], pr[0][1]), pack2<KV>(pr[0][2], pr[0][3]),
-                                    pack2<KV>(pr[1][0], pr[1][1]), pack2<KV>(pr[1][2], pr[1][3])};
+            // P = hi + lo in two 16-bit parts (lo = rn(P - hi), the difference
+            // exact in fp32): a row that sees two or three tokens would
+            // otherwise carry the 2^-9 rounding of a bf16 weight into its output
+            uint32_t pa[4], pl[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float x = pr[k >> 1][2 * (k & 1)], y = pr[k >> 1][2 * (k & 1) + 1];
+                pa[k] = pack2<KV>(x, y);
+                const float2 r = unpack2(KV{}, pa[k]);
+                pl[k] = pack2<KV>(x - r.x, y - r.y);
+            }
             // O = O * alpha + P V
 #pragma unroll
             for (int nd = 0; nd < D / 8; ++nd) {
@@ -443,6 +452,8 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 ldsm_x4_trans(smem_addr(vt + (ndp / 4) * C::SUB) + swz(tok, c), b0, b1, b2, b3);
                 mma16816<KV>(o[2 * ndp], pa, b0, b1);
                 mma16816<KV>(o[2 * ndp + 1], pa, b2, b3);
+                mma16816<KV>(o[2 * ndp], pl, b0, b1);
+                mma16816<KV>(o[2 * ndp + 1], pl, b2, b3);
             }
         }
         // release the stage; generic-proxy writes (the zeroing) must be

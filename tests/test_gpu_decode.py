@@ -161,6 +161,30 @@ def _full(name):
     return _cache[key]
 
 
+@pytest.mark.parametrize("spread", [False, True])
+def test_int8_large_value_scales(spread):
+    """INT8 V scales far above the fp16 range of the probabilities' carrier:
+    2^24 everywhere (the output scales exactly), or 2^20 .. 2^24 varying by
+    block, so that a piece meets ever larger scales midway."""
+    import torch
+    cfg = variant(CONFIGS["gqa8b_int8"], batch=6, len_groups=((6, 100, 700),))
+    w = make_workload(cfg)
+    g, o = GpuCase(w), OracleCase(w)
+    blk = np.arange(w.num_blocks)
+    f = 2.0 ** (20 + (blk * 7) % 5) if spread else np.full(w.num_blocks, 2.0 ** 24)
+    o.vs = (o.vs.astype(np.float64) * f[:, None]).astype(np.float32)
+    g.v_scales.copy_(torch.from_numpy(o.vs).cuda())
+    want = o.attention()
+    for parts in (0, 7):
+        out, _ = g.decode(num_parts=parts)
+        _sync()
+        got = out_to_f64(out)
+        assert np.isfinite(got).all()
+        err = np.abs(got - want)
+        assert (err <= 2e-2 * 2.0 ** 20 + 1e-2 * np.abs(want)).all(), (spread, parts, err.max())
+    assert int(g.status.item()) == 0
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa8b", "gqa8b_int8", "skewed"])
 def test_decode_full_size_sampled(name):

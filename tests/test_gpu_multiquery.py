@@ -99,6 +99,25 @@ def test_variable_query_counts_including_empty():
         assert_attention_close(out_to_f64(out), want, False, f"varlen parts={parts}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("n", [48, 33])
+def test_first_prefill_chunk_from_position_zero(dtype, n):
+    """The whole context is new (L == n): query i sees only tokens 0..i, so
+    the first rows average two or three values and expose any rounding of
+    the probabilities."""
+    cfg = variant(CONFIGS["prefill_chunk"], batch=4, q_len=n, max_len=64,
+                  len_groups=((4, n, n),), kv_dtype=dtype, q_dtype=dtype, src_dtype=dtype)
+    w = make_workload(cfg)
+    assert (w.context_lens == n).all()
+    g, o = GpuCase(w), OracleCase(w)
+    want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
+                                             w.context_lens, w.cfg.softmax_scale)
+    for parts in (0, 5):
+        out = run_mq(g, w.q, w.cu_q, n, parts)
+        _sync()
+        assert_attention_close(out_to_f64(out), want, False, f"{dtype} from 0 parts={parts}")
+
+
 def test_too_many_queries_are_flagged_not_written():
     import torch
     from paged_kv_decode_05_gb300 import binding as B
