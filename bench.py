@@ -448,34 +448,64 @@ def run_native(args):
 
 
 def _e2e(st, w, cfg, ws, parts, device, K, world):
-    """Same metric through the C ABI, with the step's inputs copied from pinned
-    host memory and the output copied back inside the timed region."""
+    """Same metric through the C ABI, with every step's inputs copied from
+    pinned host memory and its output copied back inside the timed region.
+
+    Served the way a decode loop runs: the inputs and the output are double
+    buffered on the device, the host-to-device copies of step n+1 run on one
+    stream and the device-to-host copy of step n on another while step n+1
+    computes; events keep a buffer from being refilled before the step that
+    reads it has finished, or overwritten before its copy-out has."""
     import torch
     names = ["q", "k_step", "v_step", "step_slots", "block_tables", "context_lens"]
     host = {n: st[n].cpu().pin_memory() for n in names}
     out_host = torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = out_host.numel() * out_host.element_size()
-    for _ in range(3):
-        for n in names:
-            st[n].copy_(host[n], non_blocking=True)
-        _step(st, cfg, ws, parts)
-        out_host.copy_(st["out"], non_blocking=True)
+    sets = [dict(st), dict(st)]
+    for n in names + ["out"]:
+        sets[1][n] = torch.empty_like(st[n])
+    comp = torch.cuda.current_stream(device)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ready = [torch.cuda.Event() for _ in range(2)]    # inputs of the set copied in
+    done = [torch.cuda.Event() for _ in range(2)]     # the step using the set finished
+    drained = [torch.cuda.Event() for _ in range(2)]  # the set's output copied out
+
+    def step(n):
+        i = n % 2
+        with torch.cuda.stream(up):
+            if n >= 2:
+                up.wait_event(done[i])
+            for name in names:
+                sets[i][name].copy_(host[name], non_blocking=True)
+            ready[i].record(up)
+        comp.wait_event(ready[i])
+        if n >= 2:
+            comp.wait_event(drained[i])
+        _step(sets[i], cfg, ws, parts)
+        done[i].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(done[i])
+            out_host.copy_(sets[i]["out"], non_blocking=True)
+            drained[i].record(down)
+
+    for n in range(4):
+        step(n)
     torch.cuda.synchronize(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(K):
-        for n in names:
-            st[n].copy_(host[n], non_blocking=True)
-        _step(st, cfg, ws, parts)
-        out_host.copy_(st["out"], non_blocking=True)
-    b.record()
+    a.record(comp)
+    for n in range(K):
+        step(n)
+    comp.wait_event(drained[(K - 1) % 2])
+    b.record(comp)
     torch.cuda.synchronize(device)
     ms = reduce_max(a.elapsed_time(b), world, device)
     alg = algorithmic_bytes(cfg, w.context_lens)
     return {"value": round(alg * world / (ms / 1e3 / K) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K,
-            "ms_per_step": round(ms / K, 6)}
+            "ms_per_step": round(ms / K, 6),
+            "how": "inputs and output double buffered; copies on two side streams overlap "
+                   "the neighbouring steps' kernels"}
 
 
 def run_reference(args):
