@@ -145,12 +145,6 @@ __global__ void i8_absmax_kernel(I8Args a) {
     }
 }
 
-__device__ __forceinline__ int quant_code(float x, float s) {
-    if (s == 0.f) return 0;
-    const int q = __float2int_rn(__fdiv_rn(x, s));  // IEEE divide, ties-to-even
-    return max(-127, min(127, q));
-}
-
 // Settle one (block, kv_head) tile's scale; requantise its codes on growth.
 __device__ __forceinline__ void settle_tile(int8_t* cache, float* scales, uint32_t amax_bits,
                                            long long t, int D) {
@@ -166,15 +160,7 @@ __device__ __forceinline__ void settle_tile(int8_t* cache, float* scales, uint32
         uint32_t* words = reinterpret_cast<uint32_t*>(cache + t * kBlockSize * D);
         const int n_words = kBlockSize * D / 4;
         for (int w = threadIdx.x & 31; w < n_words; w += 32) {
-            const uint32_t in = words[w];
-            uint32_t out = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int q = int(int8_t(in >> (8 * b)));
-                const float r = __fdiv_rn(__fmul_rn(float(q), s_o), s);
-                out |= (uint32_t(__float2int_rn(r)) & 0xffu) << (8 * b);
-            }
-            words[w] = out;
+            words[w] = requant_word(words[w], s_o, s);
         }
     }
     __syncwarp();

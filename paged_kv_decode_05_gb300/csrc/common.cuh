@@ -104,6 +104,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// ------------------------------------------------------------ INT8 codes ---
+// New code of value x under scale s: clamp(rne(x / s), -127, 127) with an
+// IEEE divide; 0 when s == 0.
+__device__ __forceinline__ int quant_code(float x, float s) {
+    if (s == 0.f) return 0;
+    const int q = __float2int_rn(__fdiv_rn(x, s));  // IEEE divide, ties-to-even
+    return max(-127, min(127, q));
+}
+// Four stored codes re-expressed under a grown scale: rne((q * s_o) / s),
+// multiply then divide, each IEEE-rounded in fp32.
+__device__ __forceinline__ uint32_t requant_word(uint32_t in, float s_o, float s) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int q = int(int8_t(in >> (8 * b)));
+        const float r = __fdiv_rn(__fmul_rn(float(q), s_o), s);
+        out |= (uint32_t(__float2int_rn(r)) & 0xffu) << (8 * b);
+    }
+    return out;
+}
+
 // ------------------------------------------------------------- mbarrier ---
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -146,6 +167,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// Order this thread's generic-proxy writes to shared memory before later
+// asynchronous-proxy (TMA) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------ bulk copy ---

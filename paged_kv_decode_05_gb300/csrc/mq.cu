@@ -161,9 +161,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tma
                  :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
                  : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Byte offset of (row r, 16-byte chunk c) inside one 16 x 128-byte sub-tile
 // written by TMA with the 128-byte swizzle (chunk index XOR row % 8).
@@ -440,10 +437,13 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 const float2 r = unpack2(KV{}, pa[k]);
                 pl[k] = pack2<KV>(x - r.x, y - r.y);
             }
-            // O = O * alpha + P V
+            // O = O * alpha + P V (the rescale only when some running max moved;
+            // the vote is warp-uniform)
+            if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                o[nd][0] *= a0; o[nd][1] *= a0; o[nd][2] *= a1; o[nd][3] *= a1;
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    o[nd][0] *= a0; o[nd][1] *= a0; o[nd][2] *= a1; o[nd][3] *= a1;
+                }
             }
 #pragma unroll
             for (int ndp = 0; ndp < D / 16; ++ndp) {
