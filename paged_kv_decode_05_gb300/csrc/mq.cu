@@ -465,6 +465,427 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
     if (!aborted && pb >= 0) finalize();
 }
 
+// ------------------------------------------------- tcgen05 row-tile kernel ---
+// Long query runs (prefill chunks): a CTA owns one (sequence, kv head, tile of
+// 128 rows), rows = (query, head) pairs, and walks the tile's visible tokens in
+// chunks of 64 (four blocks) on the 5th-generation tensor cores:
+//   S = Q K^T      tcgen05.mma kind::f16, M = 128, N = 64, K = D, fp32 in TMEM
+//   softmax        one thread per row reads its S row from TMEM (no shuffles)
+//   O += P V       tcgen05.mma, M = 128, N = D, K = 64; P from shared memory
+//                  (hi + lo 16-bit parts), V read MN-major straight from its
+//                  TMA tile; O stays in TMEM for the whole tile.
+// Warp 0 produces (TMA of K/V chunks into NSTG stages), warp 1 issues the MMAs
+// and owns the TMEM allocation, warps 2-5 run the softmax and the epilogue.
+// Operands in shared memory use the 128-byte swizzle (TMA writes K/V that way;
+// Q and P are written by threads in the same pattern). O is rescaled only when
+// a row's running maximum grows by more than 2^8 (then exactly); in between P
+// is taken against the older maximum, and O and l always share it.
+
+constexpr int kTcRows = 128;       // rows per tile (TMEM lanes)
+constexpr int kTcChunk = 64;       // tokens per chunk
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 192;
+constexpr float kTcLazy = 8.0f;    // log2 growth of the max tolerated before rescaling O
+
+template <int D>
+struct TcCfg {
+    static constexpr int NH = D / 64;                     // 128-byte column halves
+    static constexpr int HALF = kTcChunk * 128;           // one half of a K or V chunk (8 KB)
+    static constexpr int KV_STAGE = 2 * NH * HALF;        // K halves then V halves
+    static constexpr int QHALF = kTcRows * 128;           // one half of the Q tile (16 KB)
+    static constexpr int PBYTES = kTcRows * kTcChunk * 2; // one P part (16 KB)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_KV = OFF_Q + NH * QHALF;
+    static constexpr int OFF_P = OFF_KV + kTcStages * KV_STAGE;   // P hi, then P lo
+    static constexpr int OFF_BAR = OFF_P + 2 * PBYTES;
+    // mbarriers: kv_full[S], kv_empty[S], s_full[2], p_full, o_done, drain
+    static constexpr int NBAR = 2 * kTcStages + 5;
+    static constexpr int OFF_MASK = OFF_BAR + NBAR * 8;           // int per stage
+    static constexpr int OFF_MISC = OFF_MASK + kTcStages * 4;     // tmem base, abort flag
+    static constexpr int BYTES = OFF_MISC + 16 + 1024;            // + alignment slack
+    static constexpr int TMEM_COLS = 256;                         // S x2 (64 each) + O (D <= 128)
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0 && HALF % 1024 == 0, "swizzle atoms");
+};
+
+// Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
+// offsets in 16-byte units, descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return uint64_t((addr >> 4) & 0x3fff) | (uint64_t((lbo >> 4) & 0x3fff) << 16) |
+           (uint64_t((sbo >> 4) & 0x3fff) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+// Instruction descriptor, kind::f16 with fp32 accumulation: operand type
+// (0 fp16, 1 bf16) for A and B, B K-major (0) or N-major (1), N and M.
+__device__ __forceinline__ uint32_t tc_idesc(uint32_t ab_type, uint32_t b_major, uint32_t n,
+                                             uint32_t m) {
+    return (1u << 4) | (ab_type << 7) | (ab_type << 10) | (b_major << 16) | ((n >> 3) << 17) |
+           ((m >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive on `bar` once all tcgen05 operations this thread issued have completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tc_ld32(uint32_t addr, float* v) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+                 "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31},"
+                 " [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(addr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_st32(uint32_t addr, const float* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                 "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
+                 "%30,%31,%32};"
+                 :: "r"(addr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                    "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+                    "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                    "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+                    "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])),
+                    "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                    "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+                    "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+                    "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+                    "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+                    "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])),
+                    "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+                    "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+                    "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+                    "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+                    "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+template <typename KV, int D, int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+             const MqParams p) {
+    using C = TcCfg<D>;
+    constexpr int QPT = kTcRows / G;   // queries per tile
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* kv_full = bars;
+    uint64_t* kv_empty = bars + kTcStages;
+    uint64_t* s_full = bars + 2 * kTcStages;
+    uint64_t* p_full = bars + 2 * kTcStages + 2;
+    uint64_t* o_done = bars + 2 * kTcStages + 3;
+    uint64_t* drain = bars + 2 * kTcStages + 4;
+    int* smask = reinterpret_cast<int*>(smem + C::OFF_MASK);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    griddep_wait();
+    griddep_launch_dependents();
+    // unit: (sequence b, kv head, tile t); heavier (later) tiles first
+    const int tmax = p.tmax;
+    const long long unit = blockIdx.x;
+    const int t = tmax - 1 - int(unit % tmax);
+    const int kvh = int((unit / tmax) % p.hkv);
+    const int b = int(unit / ((long long)tmax * p.hkv));
+    int n, L;
+    bool bad;
+    seq_shape_raw(p.cu_q, p.context_lens, b, p.mb, p.max_q, n, L, bad);
+    if (bad && threadIdx.x == 0 && kvh == 0 && t == 0) flag_status(p.status, PKV_DEV_BAD_LENGTH);
+    const int q0 = t * QPT;
+    if (q0 >= n) return;   // the whole CTA leaves before any allocation
+    const int cu = p.cu_q[b];
+    const int q_last = min(n, q0 + QPT) - 1;
+    const int pos_max = L - n + q_last;                    // last token any row may see
+    const int nch = (pos_max + 1 + kTcChunk - 1) / kTcChunk;
+    const int jmax = pos_max / kBlockSize;                 // last block needed
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NBAR; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        fence_mbar_init();
+        misc[1] = 0u;   // abort flag
+    }
+    // V stages start zeroed: rows of blocks that are never loaded must not hold NaN
+    for (int i = threadIdx.x; i < kTcStages * C::KV_STAGE / 16; i += kTcThreads) {
+        const int s = i / (C::KV_STAGE / 16), off = i % (C::KV_STAGE / 16);
+        if (off >= C::NH * C::HALF / 16)
+            reinterpret_cast<uint4*>(smem + C::OFF_KV + s * C::KV_STAGE)[off] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // Q tile rows (query q0 + r / G, head r % G), zero past the sequence, in the
+    // 128-byte-swizzled K-major layout (row r at r * 128 in each half)
+    for (int i = threadIdx.x; i < kTcRows * (D / 8); i += kTcThreads) {
+        const int r = i / (D / 8), c16 = i % (D / 8);       // 16-byte chunk of the row
+        const int qi = q0 + r / G, h = r % G;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qi < n)
+            v = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                ((long long)(cu + qi) * p.hq + kvh * G + h) * D + c16 * 8);
+        const int half = c16 / 8, c = c16 % 8;
+        *reinterpret_cast<uint4*>(smem + C::OFF_Q + half * C::QHALF + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_addr((const void*)(misc + 0))), "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const uint32_t tm_o = tmem + 2 * kTcChunk;             // O columns follow the two S buffers
+
+    auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t role_bit) -> bool {
+        if (misc[1]) return false;
+        const bool ok = mbar_wait_bounded(smem_addr(bar), parity, 2000000000ull);
+        if (!ok) {
+            misc[1] = 1u;
+            flag_status(p.status, PKV_DEV_TIMEOUT | role_bit);
+        }
+        return ok;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer ---
+        if (lane == 0) {
+            for (int c = 0; c < nch; ++c) {
+                const int st = c % kTcStages;
+                if (c >= kTcStages && !wait(&kv_empty[st], ((c / kTcStages) - 1) & 1, 0x400u)) break;
+                int mask = 0, nl = 0;
+                int blk[kTcChunk / kBlockSize];
+#pragma unroll
+                for (int jj = 0; jj < kTcChunk / kBlockSize; ++jj) {
+                    const int j = c * (kTcChunk / kBlockSize) + jj;
+                    blk[jj] = -1;
+                    if (j <= jmax) {
+                        const int x = __ldg(p.block_tables + (long long)b * p.mb + j);
+                        if (unsigned(x) < unsigned(p.num_blocks)) {
+                            blk[jj] = x;
+                            mask |= 1 << jj;
+                            ++nl;
+                        } else {
+                            flag_status(p.status, PKV_DEV_BAD_BLOCK);
+                        }
+                    }
+                }
+                smask[st] = mask;
+                const uint32_t bar = smem_addr(&kv_full[st]);
+                if (nl) mbar_arrive_expect_tx(bar, uint32_t(nl * 2 * C::NH * kBlockSize * 128));
+                else mbar_arrive(bar);
+                unsigned char* sk = smem + C::OFF_KV + st * C::KV_STAGE;
+#pragma unroll
+                for (int jj = 0; jj < kTcChunk / kBlockSize; ++jj) {
+                    if (blk[jj] < 0) continue;
+                    const int y = (blk[jj] * p.hkv + kvh) * kBlockSize;
+#pragma unroll
+                    for (int h = 0; h < C::NH; ++h) {
+                        tma_load_2d(smem_addr(sk + h * C::HALF + jj * kBlockSize * 128), &tmk, 64 * h, y, bar);
+                        tma_load_2d(smem_addr(sk + (C::NH + h) * C::HALF + jj * kBlockSize * 128), &tmv,
+                                    64 * h, y, bar);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer ---
+        if (lane == 0) {
+            const uint32_t ab = std::is_same<KV, BF16>::value ? 1u : 0u;
+            const uint32_t id_s = tc_idesc(ab, 0, kTcChunk, kTcRows);   // S: B = K, K-major
+            const uint32_t id_o = tc_idesc(ab, 1, D, kTcRows);          // O: B = V, N-major
+            const uint32_t q_base = smem_addr(smem + C::OFF_Q);
+            const uint32_t p_base = smem_addr(smem + C::OFF_P);
+            auto issue_s = [&](int c) {
+                const int st = c % kTcStages;
+                const uint32_t k_base = smem_addr(smem + C::OFF_KV + st * C::KV_STAGE);
+                const uint32_t d = tmem + (c & 1) * kTcChunk;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk % 4) * 32;
+                    tc_mma(d, tc_desc(q_base + (kk / 4) * C::QHALF + off, 16, 1024),
+                           tc_desc(k_base + (kk / 4) * C::HALF + off, 16, 1024), id_s, kk > 0);
+                }
+                tc_commit(smem_addr(&s_full[c & 1]));
+            };
+            auto issue_pv = [&](int c) {
+                const int st = c % kTcStages;
+                const uint32_t v_base = smem_addr(smem + C::OFF_KV + st * C::KV_STAGE + C::NH * C::HALF);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kTcChunk / 16; ++kk)
+                        tc_mma(tm_o, tc_desc(p_base + part * C::PBYTES + kk * 32, 16, 1024),
+                               tc_desc(v_base + kk * 16 * 128, C::HALF, 1024), id_o,
+                               (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(smem_addr(&kv_empty[st]));
+                tc_commit(smem_addr(&o_done[0]));
+            };
+            bool ok = true;
+            for (int c = 0; c < nch && ok; ++c) {
+                const int st = c % kTcStages;
+                ok = wait(&kv_full[st], (c / kTcStages) & 1, 0x800u);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(c);
+                if (c > 0) {
+                    ok = wait(&p_full[0], (c - 1) & 1, 0x800u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(c - 1);
+                }
+            }
+            if (ok && wait(&p_full[0], (nch - 1) & 1, 0x800u)) {
+                tc_fence_after();
+                issue_pv(nch - 1);
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            tc_commit(smem_addr(&drain[0]));
+            mbar_wait_bounded(smem_addr(&drain[0]), 0, 2000000000ull);
+        }
+    } else {
+        // ----------------------------------------------- softmax + epilogue ---
+        const int r = 32 * (warp & 3) + lane;                 // TMEM lane = tile row
+        const uint32_t lane_addr = uint32_t(32 * (warp & 3)) << 16;
+        const int qi = q0 + r / G;
+        const bool rv = qi < n;
+        const int pos = L - n + qi;                            // last token this row sees
+        float m = -INFINITY, l = 0.f;
+        unsigned char* ph = smem + C::OFF_P + r * 128;
+        const int last_blk_tok = ((L - 1) / kBlockSize) * kBlockSize;   // first token of the last block
+        // ok stays warp-uniform; after an abort every iteration still reaches
+        // the named barrier, so no softmax warp can be left waiting there
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const int st = c % kTcStages;
+            const int tok0 = c * kTcChunk;
+            if (ok) ok = __all_sync(kFull, wait(&s_full[c & 1], (c >> 1) & 1, 0x1000u));
+            // the producer's block mask and TMA writes of this stage, observed directly
+            if (ok) ok = __all_sync(kFull, wait(&kv_full[st], (c / kTcStages) & 1, 0x1000u));
+            float s[kTcChunk];
+            float mx = -INFINITY;
+            int mask = 0;
+            if (ok) {
+                tc_fence_after();
+                tc_ld32(tmem + lane_addr + (c & 1) * kTcChunk, s);
+                tc_ld32(tmem + lane_addr + (c & 1) * kTcChunk + 32, s + 32);
+                mask = smask[st];
+#pragma unroll
+                for (int i = 0; i < kTcChunk; ++i) {
+                    const int tok = tok0 + i;
+                    const bool vis = rv && tok <= pos && ((mask >> (i / kBlockSize)) & 1);
+                    s[i] = vis ? s[i] * p.qscale : -INFINITY;
+                    mx = fmaxf(mx, s[i]);
+                }
+                // P and O are free again once the previous chunk's P.V completed
+                if (c > 0) ok = __all_sync(kFull, wait(&o_done[0], (c - 1) & 1, 0x1000u));
+            }
+            if (ok) {
+                tc_fence_after();
+                const bool grow = mx > m + kTcLazy || (m == -INFINITY && mx > -INFINITY);
+                if (c > 0 && __any_sync(kFull, grow && m > -INFINITY)) {
+                    // rescale this row's O (warp-collective TMEM access; others by 1)
+                    const float a = (grow && m > -INFINITY) ? fast_exp2(m - mx) : 1.f;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        float o[32];
+                        tc_ld32(tm_o + lane_addr + c0, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= a;
+                        tc_st32(tm_o + lane_addr + c0, o);
+                    }
+                    if (grow && m > -INFINITY) l *= a;
+                }
+                if (grow) m = mx;
+                // P = exp2(s - m) as hi + lo 16-bit parts, written swizzled (row r)
+#pragma unroll
+                for (int c16 = 0; c16 < kTcChunk / 8; ++c16) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float y0 = s[c16 * 8 + 2 * e], y1 = s[c16 * 8 + 2 * e + 1];
+                        const float x0 = y0 == -INFINITY ? 0.f : fast_exp2(y0 - m);
+                        const float x1 = y1 == -INFINITY ? 0.f : fast_exp2(y1 - m);
+                        l += x0 + x1;
+                        hw[e] = pack2<KV>(x0, x1);
+                        const float2 rr = unpack2(KV{}, hw[e]);
+                        lw[e] = pack2<KV>(x0 - rr.x, x1 - rr.y);
+                    }
+                    const uint32_t off = uint32_t((c16 ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(ph + C::PBYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                // V rows past the context in the sequence's last block may hold
+                // anything (NaN): zero them before P.V reads them
+                if (last_blk_tok >= tok0 && last_blk_tok < tok0 + kTcChunk &&
+                    L < last_blk_tok + kBlockSize) {
+                    const int jj = (last_blk_tok - tok0) / kBlockSize;
+                    if ((mask >> jj) & 1) {
+                        const int r0 = L - last_blk_tok;                 // first stale row of the block
+                        const int nrow = kBlockSize - r0;
+                        unsigned char* vb = smem + C::OFF_KV + st * C::KV_STAGE + C::NH * C::HALF;
+                        for (int i = r; i < nrow * C::NH * 8; i += kTcRows) {
+                            const int row = i / (C::NH * 8), rem = i % (C::NH * 8);
+                            const int h = rem / 8, c8 = rem % 8;       // whole rows: swizzle irrelevant
+                            *reinterpret_cast<uint4*>(vb + h * C::HALF + (jj * kBlockSize + r0 + row) * 128 + c8 * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            tc_named_sync(1, kTcRows);
+            if (r == 0) mbar_arrive(smem_addr(&p_full[0]));
+        }
+        // epilogue: O / l for the row, in q's dtype
+        if (ok) ok = __all_sync(kFull, wait(&o_done[0], (nch - 1) & 1, 0x1000u));
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + ((long long)(cu + qi) * p.hq + kvh * G + r % G) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tc_ld32(tm_o + lane_addr + c0, o);
+                if (rv) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack2<KV>(o[2 * i] * inv, o[2 * i + 1] * inv);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::TMEM_COLS));
+}
+
 // ---------------------------------------------------------------- combine ---
 struct MqCombine {
     const float* part_o;
@@ -628,6 +1049,34 @@ bool mq_pick_d(int D, int G, int nw, MqOps* o) {
     return false;
 }
 
+// tcgen05 row-tile path: launchers by cache type, head dim and group size.
+using TcLaunch = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const MqParams&, int,
+                                 cudaStream_t);
+template <typename KV, int D, int G>
+cudaError_t tc_launch(const CUtensorMap& k, const CUtensorMap& v, const MqParams& p, int grid,
+                      cudaStream_t st) {
+    const int smem = TcCfg<D>::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(mq_tc_kernel<KV, D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(mq_tc_kernel<KV, D, G>, dim3(grid), dim3(kTcThreads), size_t(smem), st, k, v, p);
+}
+template <typename KV, int D>
+TcLaunch tc_pick_g(int G) {
+    switch (G) {
+        case 1: return tc_launch<KV, D, 1>;
+        case 2: return tc_launch<KV, D, 2>;
+        case 4: return tc_launch<KV, D, 4>;
+    }
+    return nullptr;
+}
+template <typename KV>
+TcLaunch tc_pick(int D, int G) {
+    if (D == 128) return tc_pick_g<KV, 128>(G);
+    if (D == 64) return tc_pick_g<KV, 64>(G);
+    return nullptr;
+}
+
 struct MqPlan {
     MqOps ops;
     int G, nw, tmax;
@@ -721,6 +1170,28 @@ extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, cons
     if (!encode_cache_map(&tk, k_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows) ||
         !encode_cache_map(&tv, v_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows))
         return PKV_ERR_CUDA;
+    // Query runs that fill 128-row tiles take the tcgen05 kernel (no split,
+    // no combine, no workspace); shorter ones the mma.sync kernel below.
+    const TcLaunch tc = ((long long)max_q_len * pl.G >= kTcRows && mq_aligned(q, 16) &&
+                         mq_aligned(out, 16))
+                            ? (cache->kv_dtype == PKV_BF16 ? tc_pick<BF16>(cache->head_dim, pl.G)
+                                                           : tc_pick<F16>(cache->head_dim, pl.G))
+                            : nullptr;
+    if (tc) {
+        MqParams p;
+        p.q = q; p.cu_q = cu_q; p.block_tables = block_tables; p.context_lens = context_lens;
+        p.out = out; p.part_o = nullptr; p.part_ml = nullptr; p.ws_prefix = nullptr;
+        p.status = dev_status;
+        p.batch = batch; p.hq = num_q_heads; p.hkv = cache->num_kv_heads;
+        p.mb = max_blocks_per_seq; p.num_blocks = cache->num_blocks; p.workers = 0;
+        p.tmax = int(((long long)max_q_len * pl.G + kTcRows - 1) / kTcRows);
+        p.max_q = max_q_len;
+        p.qscale = softmax_scale * kMqLog2e;
+        const long long grid = (long long)batch * p.hkv * p.tmax;
+        if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+        if (tc(tk, tv, p, int(grid), stream) != cudaSuccess) return PKV_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    }
     char* ws = static_cast<char*>(workspace);
     MqParams p;
     p.q = q; p.cu_q = cu_q; p.block_tables = block_tables; p.context_lens = context_lens;

@@ -118,6 +118,37 @@ def test_first_prefill_chunk_from_position_zero(dtype, n):
         assert_attention_close(out_to_f64(out), want, False, f"{dtype} from 0 parts={parts}")
 
 
+# Query runs that fill 128-row tiles (q_len * g >= 128) take the tcgen05 kernel.
+TC = {
+    "g4_d128_bf16": variant(CONFIGS["prefill_chunk"], batch=3, q_len=64, max_len=2000,
+                            len_groups=((3, 64, 2000),)),
+    "g2_d64_f16": variant(CONFIGS["prefill_chunk"], batch=3, num_q_heads=8, num_kv_heads=4,
+                          head_dim=64, kv_dtype="f16", q_dtype="f16", src_dtype="f16", q_len=100,
+                          max_len=1200, len_groups=((3, 100, 1200),)),
+    "g1_d128_two_tiles": variant(CONFIGS["prefill_chunk"], batch=2, num_q_heads=4, num_kv_heads=4,
+                                 q_len=150, max_len=700, len_groups=((2, 150, 700),)),
+    # scores spread over a wide range: running maxima jump by more than 2^8
+    "g4_wide_scores": variant(CONFIGS["prefill_chunk"], batch=2, q_len=40, max_len=1500,
+                              len_groups=((2, 40, 1500),), q_std=6.0),
+}
+
+
+@pytest.mark.parametrize("name", list(TC))
+def test_tensor_core_row_tiles(name):
+    cfg = TC[name]
+    assert cfg.q_len * (cfg.num_q_heads // cfg.num_kv_heads) >= 128
+    w = make_workload(cfg)
+    g, o = GpuCase(w), OracleCase(w)
+    want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
+                                             w.context_lens, w.cfg.softmax_scale)
+    out = run_mq(g, w.q, w.cu_q, w.cfg.q_len)
+    _sync()
+    got = out_to_f64(out)
+    assert np.isfinite(got).all()
+    assert_attention_close(got, want, False, name)
+    assert int(g.status.item()) == 0
+
+
 def test_too_many_queries_are_flagged_not_written():
     import torch
     from paged_kv_decode_05_gb300 import binding as B
