@@ -578,6 +578,22 @@ __device__ __forceinline__ void tc_st32(uint32_t addr, const float* v) {
                  : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// Bounded wait that lets the thread sleep in the barrier (suspend-time hint)
+// instead of spinning: waiting warps then leave the issue slots to the
+// producer and MMA threads that share their sub-partitions.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 20); ++it) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(ok) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
+        if (ok) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
 __device__ __forceinline__ void tc_named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
@@ -659,7 +675,7 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 
     auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t role_bit) -> bool {
         if (misc[1]) return false;
-        const bool ok = mbar_wait_bounded(smem_addr(bar), parity, 2000000000ull);
+        const bool ok = tc_wait(smem_addr(bar), parity, 2000000000ull);
         if (!ok) {
             misc[1] = 1u;
             flag_status(p.status, PKV_DEV_TIMEOUT | role_bit);
@@ -716,27 +732,33 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             const uint32_t id_o = tc_idesc(ab, 1, D, kTcRows);          // O: B = V, N-major
             const uint32_t q_base = smem_addr(smem + C::OFF_Q);
             const uint32_t p_base = smem_addr(smem + C::OFF_P);
+            // Descriptors differ only in their start-address field (16-byte
+            // units, low bits): build each base once, then add offsets.
+            const uint64_t dq = tc_desc(q_base, 16, 1024);
+            const uint64_t dp = tc_desc(p_base, 16, 1024);
+            const uint64_t dk0 = tc_desc(smem_addr(smem + C::OFF_KV), 16, 1024);
+            const uint64_t dv0 = tc_desc(smem_addr(smem + C::OFF_KV + C::NH * C::HALF), C::HALF, 1024);
             auto issue_s = [&](int c) {
                 const int st = c % kTcStages;
-                const uint32_t k_base = smem_addr(smem + C::OFF_KV + st * C::KV_STAGE);
+                const uint64_t dk = dk0 + uint64_t(st * (C::KV_STAGE >> 4));
                 const uint32_t d = tmem + (c & 1) * kTcChunk;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk % 4) * 32;
-                    tc_mma(d, tc_desc(q_base + (kk / 4) * C::QHALF + off, 16, 1024),
-                           tc_desc(k_base + (kk / 4) * C::HALF + off, 16, 1024), id_s, kk > 0);
+                    const uint32_t off = ((kk / 4) * C::QHALF + (kk % 4) * 32) >> 4;
+                    const uint32_t offk = ((kk / 4) * C::HALF + (kk % 4) * 32) >> 4;
+                    tc_mma(d, dq + off, dk + offk, id_s, kk > 0);
                 }
                 tc_commit(smem_addr(&s_full[c & 1]));
             };
             auto issue_pv = [&](int c) {
                 const int st = c % kTcStages;
-                const uint32_t v_base = smem_addr(smem + C::OFF_KV + st * C::KV_STAGE + C::NH * C::HALF);
+                const uint64_t dv = dv0 + uint64_t(st * (C::KV_STAGE >> 4));
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kTcChunk / 16; ++kk)
-                        tc_mma(tm_o, tc_desc(p_base + part * C::PBYTES + kk * 32, 16, 1024),
-                               tc_desc(v_base + kk * 16 * 128, C::HALF, 1024), id_o,
+                        tc_mma(tm_o, dp + uint64_t((part * C::PBYTES + kk * 32) >> 4),
+                               dv + uint64_t((kk * 16 * 128) >> 4), id_o,
                                (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(smem_addr(&kv_empty[st]));
                 tc_commit(smem_addr(&o_done[0]));
