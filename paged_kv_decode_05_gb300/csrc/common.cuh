@@ -157,14 +157,25 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
 // of the global timer or 2^26 polls, whichever comes first (the poll cap
-// bounds the wait even if the timer were not to advance).
+// bounds the wait even if the timer were not to advance). Between polls the
+// thread sleeps in the barrier.
+// As mbar_try_wait, but the thread may sleep in the barrier (suspend-time hint
+// of 1 ms) until the phase completes, leaving the issue slots to other warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1; !mbar_try_wait(bar, parity); ++it) {
+    for (uint32_t it = 1; !mbar_try_wait_sleep(bar, parity); ++it) {
         if (it >= (1u << 26)) return false;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
