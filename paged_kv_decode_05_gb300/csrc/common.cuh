@@ -155,10 +155,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
-// of the global timer or 2^26 polls, whichever comes first (the poll cap
-// bounds the wait even if the timer were not to advance). Between polls the
-// thread sleeps in the barrier.
 // As mbar_try_wait, but the thread may sleep in the barrier (suspend-time hint
 // of 1 ms) until the phase completes, leaving the issue slots to other warps.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
@@ -169,6 +165,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
                  : "=r"(ok) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
     return ok != 0;
 }
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// of the global timer or 2^26 polls, whichever comes first (the poll cap
+// bounds the wait even if the timer were not to advance). Between polls the
+// thread sleeps in the barrier.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
