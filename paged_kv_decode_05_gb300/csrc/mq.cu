@@ -578,22 +578,6 @@ __device__ __forceinline__ void tc_st32(uint32_t addr, const float* v) {
                  : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-// Bounded wait that lets the thread sleep in the barrier (suspend-time hint)
-// instead of spinning: waiting warps then leave the issue slots to the
-// producer and MMA threads that share their sub-partitions.
-__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 0; it < (1u << 20); ++it) {
-        uint32_t ok;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(ok) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
-        if (ok) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
-    }
-    return false;
-}
 __device__ __forceinline__ void tc_named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
@@ -675,7 +659,7 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 
     auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t role_bit) -> bool {
         if (misc[1]) return false;
-        const bool ok = tc_wait(smem_addr(bar), parity, 2000000000ull);
+        const bool ok = mbar_wait_bounded(smem_addr(bar), parity, 2000000000ull);
         if (!ok) {
             misc[1] = 1u;
             flag_status(p.status, PKV_DEV_TIMEOUT | role_bit);
