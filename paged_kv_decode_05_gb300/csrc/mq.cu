@@ -475,7 +475,8 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 //                  (hi + lo 16-bit parts), V read MN-major straight from its
 //                  TMA tile; O stays in TMEM for the whole tile.
 // Warp 0 produces (TMA of K/V chunks into NSTG stages), warp 1 issues the MMAs
-// and owns the TMEM allocation, warps 2-5 run the softmax and the epilogue.
+// and owns the TMEM allocation, warps 2-9 run the softmax and the epilogue,
+// two threads per row (32 score columns and D/2 output columns each).
 // Operands in shared memory use the 128-byte swizzle (TMA writes K/V that way;
 // Q and P are written by threads in the same pattern). O is rescaled only when
 // a row's running maximum grows by more than 2^8 (then exactly); in between P
@@ -484,7 +485,8 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 constexpr int kTcRows = 128;       // rows per tile (TMEM lanes)
 constexpr int kTcChunk = 64;       // tokens per chunk
 constexpr int kTcStages = 3;
-constexpr int kTcThreads = 192;
+constexpr int kTcSoftmax = 256;    // two threads per row, 32 score columns each
+constexpr int kTcThreads = 64 + kTcSoftmax;
 constexpr float kTcLazy = 8.0f;    // log2 growth of the max tolerated before rescaling O
 
 template <int D>
@@ -501,7 +503,8 @@ struct TcCfg {
     // mbarriers: kv_full[S], kv_empty[S], s_full[2], p_full, o_done, drain
     static constexpr int NBAR = 2 * kTcStages + 5;
     static constexpr int OFF_MASK = OFF_BAR + NBAR * 8;           // int per stage
-    static constexpr int OFF_MISC = OFF_MASK + kTcStages * 4;     // tmem base, abort flag
+    static constexpr int OFF_XM = (OFF_MASK + kTcStages * 4 + 15) / 16 * 16;   // [2][128] float
+    static constexpr int OFF_MISC = OFF_XM + 2 * kTcRows * 4;      // tmem base, abort flag
     static constexpr int BYTES = OFF_MISC + 16 + 1024;            // + alignment slack
     static constexpr int TMEM_COLS = 256;                         // S x2 (64 each) + O (D <= 128)
     static_assert(D == 64 || D == 128, "head_dim");
@@ -771,61 +774,72 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         }
     } else {
         // ----------------------------------------------- softmax + epilogue ---
+        // Two threads per row: hf picks the row's score columns [32 hf, 32 hf + 32)
+        // of each chunk and output columns [hf D/2, (hf + 1) D/2). Warps w and
+        // w + 4 share TMEM lanes 32 (w % 4) .. + 31.
+        const int hf = (warp - 2) >> 2;
         const int r = 32 * (warp & 3) + lane;                 // TMEM lane = tile row
+        const int ts = hf * kTcRows + r;                       // 0 .. 255
         const uint32_t lane_addr = uint32_t(32 * (warp & 3)) << 16;
         const int qi = q0 + r / G;
         const bool rv = qi < n;
         const int pos = L - n + qi;                            // last token this row sees
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;                          // l: this half's partial sum
+        float* xm = reinterpret_cast<float*>(smem + C::OFF_XM);   // [half][row]
         unsigned char* ph = smem + C::OFF_P + r * 128;
         const int last_blk_tok = ((L - 1) / kBlockSize) * kBlockSize;   // first token of the last block
+        constexpr int SC = kTcChunk / 2;                       // score columns per thread
         // ok stays warp-uniform; after an abort every iteration still reaches
-        // the named barrier, so no softmax warp can be left waiting there
+        // both named barriers, so no softmax warp can be left waiting there
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const int st = c % kTcStages;
-            const int tok0 = c * kTcChunk;
+            const int tok0 = c * kTcChunk + hf * SC;
             if (ok) ok = __all_sync(kFull, wait(&s_full[c & 1], (c >> 1) & 1, 0x1000u));
             // the producer's block mask and TMA writes of this stage, observed directly
             if (ok) ok = __all_sync(kFull, wait(&kv_full[st], (c / kTcStages) & 1, 0x1000u));
-            float s[kTcChunk];
-            float mx = -INFINITY;
+            float s[SC];
+            float mh = -INFINITY;
             int mask = 0;
             if (ok) {
                 tc_fence_after();
-                tc_ld32(tmem + lane_addr + (c & 1) * kTcChunk, s);
-                tc_ld32(tmem + lane_addr + (c & 1) * kTcChunk + 32, s + 32);
+                tc_ld32(tmem + lane_addr + (c & 1) * kTcChunk + hf * SC, s);
                 mask = smask[st];
 #pragma unroll
-                for (int i = 0; i < kTcChunk; ++i) {
+                for (int i = 0; i < SC; ++i) {
                     const int tok = tok0 + i;
-                    const bool vis = rv && tok <= pos && ((mask >> (i / kBlockSize)) & 1);
+                    const bool vis = rv && tok <= pos && ((mask >> ((hf * SC + i) / kBlockSize)) & 1);
                     s[i] = vis ? s[i] * p.qscale : -INFINITY;
-                    mx = fmaxf(mx, s[i]);
+                    mh = fmaxf(mh, s[i]);
                 }
-                // P and O are free again once the previous chunk's P.V completed
-                if (c > 0) ok = __all_sync(kFull, wait(&o_done[0], (c - 1) & 1, 0x1000u));
             }
+            // the row's maximum over both halves
+            xm[ts] = mh;
+            tc_named_sync(1, kTcSoftmax);
+            const float mx = fmaxf(mh, xm[(1 - hf) * kTcRows + r]);
+            // P and O are free again once the previous chunk's P.V completed
+            if (ok && c > 0) ok = __all_sync(kFull, wait(&o_done[0], (c - 1) & 1, 0x1000u));
             if (ok) {
                 tc_fence_after();
                 const bool grow = mx > m + kTcLazy || (m == -INFINITY && mx > -INFINITY);
                 if (c > 0 && __any_sync(kFull, grow && m > -INFINITY)) {
-                    // rescale this row's O (warp-collective TMEM access; others by 1)
+                    // rescale this half of the row's O (warp-collective TMEM
+                    // access; rows that keep their maximum multiply by 1)
                     const float a = (grow && m > -INFINITY) ? fast_exp2(m - mx) : 1.f;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
                         float o[32];
-                        tc_ld32(tm_o + lane_addr + c0, o);
+                        tc_ld32(tm_o + lane_addr + hf * (D / 2) + c0, o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= a;
-                        tc_st32(tm_o + lane_addr + c0, o);
+                        tc_st32(tm_o + lane_addr + hf * (D / 2) + c0, o);
                     }
                     if (grow && m > -INFINITY) l *= a;
                 }
                 if (grow) m = mx;
                 // P = exp2(s - m) as hi + lo 16-bit parts, written swizzled (row r)
 #pragma unroll
-                for (int c16 = 0; c16 < kTcChunk / 8; ++c16) {
+                for (int c16 = 0; c16 < SC / 8; ++c16) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -837,20 +851,21 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                         const float2 rr = unpack2(KV{}, hw[e]);
                         lw[e] = pack2<KV>(x0 - rr.x, x1 - rr.y);
                     }
-                    const uint32_t off = uint32_t((c16 ^ (r & 7)) << 4);
+                    const uint32_t off = uint32_t(((hf * (SC / 8) + c16) ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4*>(ph + C::PBYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
                 // V rows past the context in the sequence's last block may hold
                 // anything (NaN): zero them before P.V reads them
-                if (last_blk_tok >= tok0 && last_blk_tok < tok0 + kTcChunk &&
+                const int ctok = c * kTcChunk;
+                if (last_blk_tok >= ctok && last_blk_tok < ctok + kTcChunk &&
                     L < last_blk_tok + kBlockSize) {
-                    const int jj = (last_blk_tok - tok0) / kBlockSize;
+                    const int jj = (last_blk_tok - ctok) / kBlockSize;
                     if ((mask >> jj) & 1) {
                         const int r0 = L - last_blk_tok;                 // first stale row of the block
                         const int nrow = kBlockSize - r0;
                         unsigned char* vb = smem + C::OFF_KV + st * C::KV_STAGE + C::NH * C::HALF;
-                        for (int i = r; i < nrow * C::NH * 8; i += kTcRows) {
+                        for (int i = ts; i < nrow * C::NH * 8; i += kTcSoftmax) {
                             const int row = i / (C::NH * 8), rem = i % (C::NH * 8);
                             const int h = rem / 8, c8 = rem % 8;       // whole rows: swizzle irrelevant
                             *reinterpret_cast<uint4*>(vb + h * C::HALF + (jj * kBlockSize + r0 + row) * 128 + c8 * 16) =
@@ -861,19 +876,23 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            tc_named_sync(1, kTcRows);
-            if (r == 0) mbar_arrive(smem_addr(&p_full[0]));
+            tc_named_sync(1, kTcSoftmax);
+            if (ts == 0) mbar_arrive(smem_addr(&p_full[0]));
         }
-        // epilogue: O / l for the row, in q's dtype
+        // epilogue: O / l for the row (both halves' sums), in q's dtype
+        xm[ts] = l;
+        tc_named_sync(1, kTcSoftmax);
+        const float lt = l + xm[(1 - hf) * kTcRows + r];
         if (ok) ok = __all_sync(kFull, wait(&o_done[0], (nch - 1) & 1, 0x1000u));
         if (ok) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + ((long long)(cu + qi) * p.hq + kvh * G + r % G) * D;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) +
+                            ((long long)(cu + qi) * p.hq + kvh * G + r % G) * D + hf * (D / 2);
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
                 float o[32];
-                tc_ld32(tm_o + lane_addr + c0, o);
+                tc_ld32(tm_o + lane_addr + hf * (D / 2) + c0, o);
                 if (rv) {
                     uint32_t w[16];
 #pragma unroll
