@@ -230,6 +230,13 @@ pkv_status pkv_decode_combine(const pkv_cache_desc *cache, int32_t batch,
  * batch <= 4096. Workspace: pkv_multiquery_workspace_size with the same
  * batch, num_q_heads, max_q_len, cache and num_parts (0 = one range per
  * resident CTA); 256-byte aligned. Caches 16-byte aligned.
+ * Two kernels serve the call: when max_q_len * g >= 128 (a prefill chunk)
+ * and q, out are 16-byte aligned, a tcgen05 / tensor-memory kernel with one
+ * CTA per (sequence, kv head, 128-row tile) and no split (num_parts and the
+ * workspace are then not used, but are still checked); otherwise an
+ * mma.sync kernel whose stream of units is cut into num_parts ranges and
+ * merged by a combine kernel through the workspace. Both compute the same
+ * causal attention within the same tolerance.
  * ------------------------------------------------------------------------ */
 size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_q_len,
                                      const pkv_cache_desc *cache, int32_t num_parts);
