@@ -466,17 +466,17 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 }
 
 // ------------------------------------------------- tcgen05 row-tile kernel ---
-// Long query runs (prefill chunks): a CTA owns one (sequence, kv head, tile of
-// 128 rows), rows = (query, head) pairs, and walks the tile's visible tokens in
-// chunks of 64 (four blocks) on the 5th-generation tensor cores:
+// Long query runs (prefill chunks): a CTA owns two tiles of 128 rows of one
+// (sequence, kv head), rows = (query, head) pairs, and walks their visible
+// tokens in chunks of 64 (four blocks) on the 5th-generation tensor cores:
 //   S = Q K^T      tcgen05.mma kind::f16, M = 128, N = 64, K = D, fp32 in TMEM
 //   softmax        one thread per row reads its S row from TMEM (no shuffles)
 //   O += P V       tcgen05.mma, M = 128, N = D, K = 64; P from shared memory
 //                  (hi + lo 16-bit parts), V read MN-major straight from its
 //                  TMA tile; O stays in TMEM for the whole tile.
 // Warp 0 produces (TMA of K/V chunks into NSTG stages), warp 1 issues the MMAs
-// and owns the TMEM allocation, warps 2-9 run the softmax and the epilogue,
-// two threads per row (32 score columns and D/2 output columns each).
+// and owns the TMEM allocation, warps 2-9 run the softmax and the epilogue
+// (four warps per tile, one thread per row).
 // Operands in shared memory use the 128-byte swizzle (TMA writes K/V that way;
 // Q and P are written by threads in the same pattern). O is rescaled only when
 // a row's running maximum grows by more than 2^8 (then exactly); in between P
@@ -485,31 +485,7 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 constexpr int kTcRows = 128;       // rows per tile (TMEM lanes)
 constexpr int kTcChunk = 64;       // tokens per chunk
 constexpr int kTcStages = 3;
-constexpr int kTcSoftmax = 256;    // two threads per row, 32 score columns each
-constexpr int kTcThreads = 64 + kTcSoftmax;
 constexpr float kTcLazy = 8.0f;    // log2 growth of the max tolerated before rescaling O
-
-template <int D>
-struct TcCfg {
-    static constexpr int NH = D / 64;                     // 128-byte column halves
-    static constexpr int HALF = kTcChunk * 128;           // one half of a K or V chunk (8 KB)
-    static constexpr int KV_STAGE = 2 * NH * HALF;        // K halves then V halves
-    static constexpr int QHALF = kTcRows * 128;           // one half of the Q tile (16 KB)
-    static constexpr int PBYTES = kTcRows * kTcChunk * 2; // one P part (16 KB)
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = OFF_Q + NH * QHALF;
-    static constexpr int OFF_P = OFF_KV + kTcStages * KV_STAGE;   // P hi, then P lo
-    static constexpr int OFF_BAR = OFF_P + 2 * PBYTES;
-    // mbarriers: kv_full[S], kv_empty[S], s_full[2], p_full, o_done, drain
-    static constexpr int NBAR = 2 * kTcStages + 5;
-    static constexpr int OFF_MASK = OFF_BAR + NBAR * 8;           // int per stage
-    static constexpr int OFF_XM = (OFF_MASK + kTcStages * 4 + 15) / 16 * 16;   // [2][128] float
-    static constexpr int OFF_MISC = OFF_XM + 2 * kTcRows * 4;      // tmem base, abort flag
-    static constexpr int BYTES = OFF_MISC + 16 + 1024;            // + alignment slack
-    static constexpr int TMEM_COLS = 256;                         // S x2 (64 each) + O (D <= 128)
-    static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0 && HALF % 1024 == 0, "swizzle atoms");
-};
 
 // Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
 // offsets in 16-byte units, descriptor version 1, 128-byte swizzle.
@@ -585,10 +561,39 @@ __device__ __forceinline__ void tc_named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
+// The two tiles (rows of tiles 2u and 2u + 1) share every K/V chunk: while
+// one tile's softmax runs, the tensor core works on the other tile's S or
+// P.V. Warps 2-5 are tile 0's softmax, warps 6-9 tile 1's. TMEM (512
+// columns): S buffers of tile x at 128 x + 64 (c % 2), O of tile x at
+// 256 + 128 x.
+constexpr int kTcThreads = 64 + 2 * kTcRows;
+
+template <int D>
+struct TcCfg {
+    static constexpr int NH = D / 64;
+    static constexpr int HALF = kTcChunk * 128;
+    static constexpr int KV_STAGE = 2 * NH * HALF;
+    static constexpr int QHALF = kTcRows * 128;
+    static constexpr int QTILE = NH * QHALF;
+    static constexpr int PBYTES = kTcRows * kTcChunk * 2;
+    static constexpr int OFF_Q = 0;                                  // tile x at OFF_Q + x QTILE
+    static constexpr int OFF_KV = OFF_Q + 2 * QTILE;
+    static constexpr int OFF_P = OFF_KV + kTcStages * KV_STAGE;      // tile x: hi, lo
+    static constexpr int OFF_BAR = OFF_P + 4 * PBYTES;
+    // kv_full[S], kv_empty[S], s_full[2 tiles][2], p_full[2], o_done[2], drain
+    static constexpr int NBAR = 2 * kTcStages + 9;
+    static constexpr int OFF_MASK = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_MISC = OFF_MASK + kTcStages * 4;
+    static constexpr int BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms");
+};
+
 template <typename KV, int D, int G>
 __global__ void __launch_bounds__(kTcThreads, 1)
 mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-             const MqParams p) {
+              const MqParams p) {
     using C = TcCfg<D>;
     constexpr int QPT = kTcRows / G;   // queries per tile
     extern __shared__ unsigned char smem_raw[];
@@ -596,56 +601,58 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* kv_full = bars;
     uint64_t* kv_empty = bars + kTcStages;
-    uint64_t* s_full = bars + 2 * kTcStages;
-    uint64_t* p_full = bars + 2 * kTcStages + 2;
-    uint64_t* o_done = bars + 2 * kTcStages + 3;
-    uint64_t* drain = bars + 2 * kTcStages + 4;
+    uint64_t* s_full = bars + 2 * kTcStages;          // [tile][buffer]
+    uint64_t* p_full = bars + 2 * kTcStages + 4;      // [tile]
+    uint64_t* o_done = bars + 2 * kTcStages + 6;      // [tile]
+    uint64_t* drain = bars + 2 * kTcStages + 8;
     int* smask = reinterpret_cast<int*>(smem + C::OFF_MASK);
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     griddep_wait();
     griddep_launch_dependents();
-    // unit: (sequence b, kv head, tile t); heavier (later) tiles first
-    const int tmax = p.tmax;
+    // unit: (sequence b, kv head, tile pair u); heavier (later) pairs first
+    const int tpair = (p.tmax + 1) / 2;
     const long long unit = blockIdx.x;
-    const int t = tmax - 1 - int(unit % tmax);
-    const int kvh = int((unit / tmax) % p.hkv);
-    const int b = int(unit / ((long long)tmax * p.hkv));
+    const int u = tpair - 1 - int(unit % tpair);
+    const int kvh = int((unit / tpair) % p.hkv);
+    const int b = int(unit / ((long long)tpair * p.hkv));
     int n, L;
     bool bad;
     seq_shape_raw(p.cu_q, p.context_lens, b, p.mb, p.max_q, n, L, bad);
-    if (bad && threadIdx.x == 0 && kvh == 0 && t == 0) flag_status(p.status, PKV_DEV_BAD_LENGTH);
-    const int q0 = t * QPT;
-    if (q0 >= n) return;   // the whole CTA leaves before any allocation
+    if (bad && threadIdx.x == 0 && kvh == 0 && u == 0) flag_status(p.status, PKV_DEV_BAD_LENGTH);
+    const int q00 = 2 * u * QPT;                           // first query of tile 0
+    if (q00 >= n) return;   // the whole CTA leaves before any allocation
+    const bool two = q00 + QPT < n;                         // tile 1 holds queries too
     const int cu = p.cu_q[b];
-    const int q_last = min(n, q0 + QPT) - 1;
+    const int q_last = min(n, q00 + (two ? 2 : 1) * QPT) - 1;
     const int pos_max = L - n + q_last;                    // last token any row may see
     const int nch = (pos_max + 1 + kTcChunk - 1) / kTcChunk;
-    const int jmax = pos_max / kBlockSize;                 // last block needed
+    const int jmax = pos_max / kBlockSize;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBAR; ++i) mbar_init(smem_addr(&bars[i]), 1);
         fence_mbar_init();
-        misc[1] = 0u;   // abort flag
+        misc[1] = 0u;
     }
-    // V stages start zeroed: rows of blocks that are never loaded must not hold NaN
     for (int i = threadIdx.x; i < kTcStages * C::KV_STAGE / 16; i += kTcThreads) {
         const int s = i / (C::KV_STAGE / 16), off = i % (C::KV_STAGE / 16);
         if (off >= C::NH * C::HALF / 16)
             reinterpret_cast<uint4*>(smem + C::OFF_KV + s * C::KV_STAGE)[off] = make_uint4(0u, 0u, 0u, 0u);
     }
-    // Q tile rows (query q0 + r / G, head r % G), zero past the sequence, in the
-    // 128-byte-swizzled K-major layout (row r at r * 128 in each half)
-    for (int i = threadIdx.x; i < kTcRows * (D / 8); i += kTcThreads) {
-        const int r = i / (D / 8), c16 = i % (D / 8);       // 16-byte chunk of the row
-        const int qi = q0 + r / G, h = r % G;
+    // both Q tiles (query q00 + R / G, head R % G for R in 0 .. 255), zero past
+    // the sequence, 128-byte-swizzled K-major
+    for (int i = threadIdx.x; i < 2 * kTcRows * (D / 8); i += kTcThreads) {
+        const int R = i / (D / 8), c16 = i % (D / 8);
+        const int x = R / kTcRows, r = R % kTcRows;
+        const int qi = q00 + R / G, h = R % G;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (qi < n)
             v = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                 ((long long)(cu + qi) * p.hq + kvh * G + h) * D + c16 * 8);
         const int half = c16 / 8, c = c16 % 8;
-        *reinterpret_cast<uint4*>(smem + C::OFF_Q + half * C::QHALF + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(smem + C::OFF_Q + x * C::QTILE + half * C::QHALF + r * 128 +
+                                  ((c ^ (r & 7)) << 4)) = v;
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -658,7 +665,6 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const uint32_t tm_o = tmem + 2 * kTcChunk;             // O columns follow the two S buffers
 
     auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t role_bit) -> bool {
         if (misc[1]) return false;
@@ -715,210 +721,172 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // ---------------------------------------------------- MMA issuer ---
         if (lane == 0) {
             const uint32_t ab = std::is_same<KV, BF16>::value ? 1u : 0u;
-            const uint32_t id_s = tc_idesc(ab, 0, kTcChunk, kTcRows);   // S: B = K, K-major
-            const uint32_t id_o = tc_idesc(ab, 1, D, kTcRows);          // O: B = V, N-major
-            const uint32_t q_base = smem_addr(smem + C::OFF_Q);
-            const uint32_t p_base = smem_addr(smem + C::OFF_P);
-            // Descriptors differ only in their start-address field (16-byte
-            // units, low bits): build each base once, then add offsets.
-            const uint64_t dq = tc_desc(q_base, 16, 1024);
-            const uint64_t dp = tc_desc(p_base, 16, 1024);
+            const uint32_t id_s = tc_idesc(ab, 0, kTcChunk, kTcRows);
+            const uint32_t id_o = tc_idesc(ab, 1, D, kTcRows);
+            const uint64_t dq0 = tc_desc(smem_addr(smem + C::OFF_Q), 16, 1024);
+            const uint64_t dp0 = tc_desc(smem_addr(smem + C::OFF_P), 16, 1024);
             const uint64_t dk0 = tc_desc(smem_addr(smem + C::OFF_KV), 16, 1024);
             const uint64_t dv0 = tc_desc(smem_addr(smem + C::OFF_KV + C::NH * C::HALF), C::HALF, 1024);
-            auto issue_s = [&](int c) {
-                const int st = c % kTcStages;
-                const uint64_t dk = dk0 + uint64_t(st * (C::KV_STAGE >> 4));
-                const uint32_t d = tmem + (c & 1) * kTcChunk;
+            auto issue_s = [&](int c, int x) {
+                const uint64_t dq = dq0 + uint64_t((x * C::QTILE) >> 4);
+                const uint64_t dk = dk0 + uint64_t((c % kTcStages) * (C::KV_STAGE >> 4));
+                const uint32_t d = tmem + x * 2 * kTcChunk + (c & 1) * kTcChunk;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * C::QHALF + (kk % 4) * 32) >> 4;
                     const uint32_t offk = ((kk / 4) * C::HALF + (kk % 4) * 32) >> 4;
                     tc_mma(d, dq + off, dk + offk, id_s, kk > 0);
                 }
-                tc_commit(smem_addr(&s_full[c & 1]));
+                tc_commit(smem_addr(&s_full[2 * x + (c & 1)]));
             };
-            auto issue_pv = [&](int c) {
-                const int st = c % kTcStages;
-                const uint64_t dv = dv0 + uint64_t(st * (C::KV_STAGE >> 4));
+            auto issue_pv = [&](int c, int x) {
+                const uint64_t dv = dv0 + uint64_t((c % kTcStages) * (C::KV_STAGE >> 4));
+                const uint64_t dp = dp0 + uint64_t((x * 2 * C::PBYTES) >> 4);
+                const uint32_t to = tmem + 4 * kTcChunk + x * 128;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kTcChunk / 16; ++kk)
-                        tc_mma(tm_o, dp + uint64_t((part * C::PBYTES + kk * 32) >> 4),
+                        tc_mma(to, dp + uint64_t((part * C::PBYTES + kk * 32) >> 4),
                                dv + uint64_t((kk * 16 * 128) >> 4), id_o,
                                (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(smem_addr(&kv_empty[st]));
-                tc_commit(smem_addr(&o_done[0]));
+                tc_commit(smem_addr(&o_done[x]));
+            };
+            auto finish = [&](int c) -> bool {   // P.V of chunk c for both tiles
+                if (!wait(&p_full[0], c & 1, 0x800u)) return false;
+                tc_fence_after();
+                issue_pv(c, 0);
+                if (two) {
+                    if (!wait(&p_full[1], c & 1, 0x800u)) return false;
+                    tc_fence_after();
+                    issue_pv(c, 1);
+                }
+                tc_commit(smem_addr(&kv_empty[c % kTcStages]));
+                return true;
             };
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
-                const int st = c % kTcStages;
-                ok = wait(&kv_full[st], (c / kTcStages) & 1, 0x800u);
+                ok = wait(&kv_full[c % kTcStages], (c / kTcStages) & 1, 0x800u);
                 if (!ok) break;
                 tc_fence_after();
-                issue_s(c);
-                if (c > 0) {
-                    ok = wait(&p_full[0], (c - 1) & 1, 0x800u);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(c - 1);
-                }
+                issue_s(c, 0);
+                if (two) issue_s(c, 1);
+                if (c > 0) ok = finish(c - 1);
             }
-            if (ok && wait(&p_full[0], (nch - 1) & 1, 0x800u)) {
-                tc_fence_after();
-                issue_pv(nch - 1);
-            }
-            // every MMA this thread issued has completed before TMEM is freed
+            if (ok) finish(nch - 1);
             tc_commit(smem_addr(&drain[0]));
             mbar_wait_bounded(smem_addr(&drain[0]), 0, 2000000000ull);
         }
     } else {
-        // ----------------------------------------------- softmax + epilogue ---
-        // Two threads per row: hf picks the row's score columns [32 hf, 32 hf + 32)
-        // of each chunk and output columns [hf D/2, (hf + 1) D/2). Warps w and
-        // w + 4 share TMEM lanes 32 (w % 4) .. + 31.
-        const int hf = (warp - 2) >> 2;
-        const int r = 32 * (warp & 3) + lane;                 // TMEM lane = tile row
-        const int ts = hf * kTcRows + r;                       // 0 .. 255
-        const uint32_t lane_addr = uint32_t(32 * (warp & 3)) << 16;
-        const int qi = q0 + r / G;
-        const bool rv = qi < n;
-        const int pos = L - n + qi;                            // last token this row sees
-        float m = -INFINITY, l = 0.f;                          // l: this half's partial sum
-        float* xm = reinterpret_cast<float*>(smem + C::OFF_XM);   // [half][row]
-        unsigned char* ph = smem + C::OFF_P + r * 128;
-        const int last_blk_tok = ((L - 1) / kBlockSize) * kBlockSize;   // first token of the last block
-        constexpr int SC = kTcChunk / 2;                       // score columns per thread
-        const bool qpos = p.qscale > 0.f;                      // max of raw scores = max of scaled
-        // ok stays warp-uniform; after an abort every iteration still reaches
-        // both named barriers, so no softmax warp can be left waiting there
-        bool ok = true;
-        for (int c = 0; c < nch; ++c) {
-            const int st = c % kTcStages;
-            const int tok0 = c * kTcChunk + hf * SC;
-            if (ok) ok = __all_sync(kFull, wait(&s_full[c & 1], (c >> 1) & 1, 0x1000u));
-            // the producer's block mask and TMA writes of this stage, observed directly
-            if (ok) ok = __all_sync(kFull, wait(&kv_full[st], (c / kTcStages) & 1, 0x1000u));
-            float s[SC];
-            float mh = -INFINITY;
-            int mask = 0;
-            bool plain = false;   // warp-uniform: raw scores, every column visible
-            if (ok) {
-                tc_fence_after();
-                tc_ld32(tmem + lane_addr + (c & 1) * kTcChunk + hf * SC, s);
-                mask = smask[st];
-                const int bits = (mask >> (hf * (SC / kBlockSize))) & ((1 << (SC / kBlockSize)) - 1);
-                plain = __all_sync(kFull, rv && pos - tok0 >= SC - 1 &&
-                                              bits == (1 << (SC / kBlockSize)) - 1) && qpos;
-                if (plain) {
-                    float mr = s[0];
+        // -------------------------------------- softmax + epilogue, per tile ---
+        const int x = (warp - 2) >> 2;                        // tile
+        if (x == 0 || two) {
+            const int r = 32 * (warp & 3) + lane;             // TMEM lane = row of the tile
+            const uint32_t lane_addr = uint32_t(32 * (warp & 3)) << 16;
+            const uint32_t tm_s = tmem + x * 2 * kTcChunk;
+            const uint32_t tm_o = tmem + 4 * kTcChunk + x * 128;
+            const int qi = q00 + x * QPT + r / G;
+            const bool rv = qi < n;
+            const int pos = L - n + qi;
+            float m = -INFINITY, l = 0.f;
+            unsigned char* ph = smem + C::OFF_P + x * 2 * C::PBYTES + r * 128;
+            const int last_blk_tok = ((L - 1) / kBlockSize) * kBlockSize;
+            bool ok = true;
+            for (int c = 0; c < nch; ++c) {
+                const int st = c % kTcStages;
+                const int tok0 = c * kTcChunk;
+                if (ok) ok = __all_sync(kFull, wait(&s_full[2 * x + (c & 1)], (c >> 1) & 1, 0x1000u));
+                if (ok) ok = __all_sync(kFull, wait(&kv_full[st], (c / kTcStages) & 1, 0x1000u));
+                float s[kTcChunk];
+                float mx = -INFINITY;
+                int mask = 0;
+                if (ok) {
+                    tc_fence_after();
+                    tc_ld32(tm_s + lane_addr + (c & 1) * kTcChunk, s);
+                    tc_ld32(tm_s + lane_addr + (c & 1) * kTcChunk + 32, s + 32);
+                    mask = smask[st];
 #pragma unroll
-                    for (int i = 1; i < SC; ++i) mr = fmaxf(mr, s[i]);
-                    mh = mr * p.qscale;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < SC; ++i) {
+                    for (int i = 0; i < kTcChunk; ++i) {
                         const int tok = tok0 + i;
-                        const bool vis = rv && tok <= pos && ((mask >> ((hf * SC + i) / kBlockSize)) & 1);
+                        const bool vis = rv && tok <= pos && ((mask >> (i / kBlockSize)) & 1);
                         s[i] = vis ? s[i] * p.qscale : -INFINITY;
-                        mh = fmaxf(mh, s[i]);
+                        mx = fmaxf(mx, s[i]);
                     }
+                    if (c > 0) ok = __all_sync(kFull, wait(&o_done[x], (c - 1) & 1, 0x1000u));
                 }
-            }
-            // the row's maximum over both halves
-            xm[ts] = mh;
-            tc_named_sync(1, kTcSoftmax);
-            const float mx = fmaxf(mh, xm[(1 - hf) * kTcRows + r]);
-            // P and O are free again once the previous chunk's P.V completed
-            if (ok && c > 0) ok = __all_sync(kFull, wait(&o_done[0], (c - 1) & 1, 0x1000u));
-            if (ok) {
-                tc_fence_after();
-                const bool grow = mx > m + kTcLazy || (m == -INFINITY && mx > -INFINITY);
-                if (c > 0 && __any_sync(kFull, grow && m > -INFINITY)) {
-                    // rescale this half of the row's O (warp-collective TMEM
-                    // access; rows that keep their maximum multiply by 1)
-                    const float a = (grow && m > -INFINITY) ? fast_exp2(m - mx) : 1.f;
+                if (ok) {
+                    tc_fence_after();
+                    const bool grow = mx > m + kTcLazy || (m == -INFINITY && mx > -INFINITY);
+                    if (c > 0 && __any_sync(kFull, grow && m > -INFINITY)) {
+                        const float a = (grow && m > -INFINITY) ? fast_exp2(m - mx) : 1.f;
 #pragma unroll
-                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                        float o[32];
-                        tc_ld32(tm_o + lane_addr + hf * (D / 2) + c0, o);
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            float o[32];
+                            tc_ld32(tm_o + lane_addr + c0, o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= a;
-                        tc_st32(tm_o + lane_addr + hf * (D / 2) + c0, o);
+                            for (int i = 0; i < 32; ++i) o[i] *= a;
+                            tc_st32(tm_o + lane_addr + c0, o);
+                        }
+                        if (grow && m > -INFINITY) l *= a;
                     }
-                    if (grow && m > -INFINITY) l *= a;
-                }
-                if (grow) m = mx;
-                // P = exp2(s - m) as hi + lo 16-bit parts, written swizzled (row r)
-                auto emit = [&](auto expo) {
+                    if (grow) m = mx;
 #pragma unroll
-                    for (int c16 = 0; c16 < SC / 8; ++c16) {
+                    for (int c16 = 0; c16 < kTcChunk / 8; ++c16) {
                         uint32_t hw[4], lw[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float x0 = expo(s[c16 * 8 + 2 * e]);
-                            const float x1 = expo(s[c16 * 8 + 2 * e + 1]);
+                            const float y0 = s[c16 * 8 + 2 * e], y1 = s[c16 * 8 + 2 * e + 1];
+                            const float x0 = y0 == -INFINITY ? 0.f : fast_exp2(y0 - m);
+                            const float x1 = y1 == -INFINITY ? 0.f : fast_exp2(y1 - m);
                             l += x0 + x1;
                             hw[e] = pack2<KV>(x0, x1);
                             const float2 rr = unpack2(KV{}, hw[e]);
                             lw[e] = pack2<KV>(x0 - rr.x, x1 - rr.y);
                         }
-                        const uint32_t off = uint32_t(((hf * (SC / 8) + c16) ^ (r & 7)) << 4);
+                        const uint32_t off = uint32_t((c16 ^ (r & 7)) << 4);
                         *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                         *reinterpret_cast<uint4*>(ph + C::PBYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
-                };
-                if (plain) {   // finite raw scores, m finite: one fma and one ex2 each
-                    const float nm = -m, qs = p.qscale;
-                    emit([&](float y) { return fast_exp2(fmaf(y, qs, nm)); });
-                } else {
-                    emit([&](float y) { return y == -INFINITY ? 0.f : fast_exp2(y - m); });
-                }
-                // V rows past the context in the sequence's last block may hold
-                // anything (NaN): zero them before P.V reads them
-                const int ctok = c * kTcChunk;
-                if (last_blk_tok >= ctok && last_blk_tok < ctok + kTcChunk &&
-                    L < last_blk_tok + kBlockSize) {
-                    const int jj = (last_blk_tok - ctok) / kBlockSize;
-                    if ((mask >> jj) & 1) {
-                        const int r0 = L - last_blk_tok;                 // first stale row of the block
-                        const int nrow = kBlockSize - r0;
-                        unsigned char* vb = smem + C::OFF_KV + st * C::KV_STAGE + C::NH * C::HALF;
-                        for (int i = ts; i < nrow * C::NH * 8; i += kTcSoftmax) {
-                            const int row = i / (C::NH * 8), rem = i % (C::NH * 8);
-                            const int h = rem / 8, c8 = rem % 8;       // whole rows: swizzle irrelevant
-                            *reinterpret_cast<uint4*>(vb + h * C::HALF + (jj * kBlockSize + r0 + row) * 128 + c8 * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                    // tile 0 zeroes V rows past the context (both tiles' P.V
+                    // follow tile 0's P in the MMA thread's order)
+                    if (x == 0 && last_blk_tok >= tok0 && last_blk_tok < tok0 + kTcChunk &&
+                        L < last_blk_tok + kBlockSize) {
+                        const int jj = (last_blk_tok - tok0) / kBlockSize;
+                        if ((mask >> jj) & 1) {
+                            const int r0 = L - last_blk_tok;
+                            const int nrow = kBlockSize - r0;
+                            unsigned char* vb = smem + C::OFF_KV + st * C::KV_STAGE + C::NH * C::HALF;
+                            for (int i = r; i < nrow * C::NH * 8; i += kTcRows) {
+                                const int row = i / (C::NH * 8), rem = i % (C::NH * 8);
+                                const int h = rem / 8, c8 = rem % 8;
+                                *reinterpret_cast<uint4*>(vb + h * C::HALF + (jj * kBlockSize + r0 + row) * 128 + c8 * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
                         }
                     }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                tc_named_sync(1 + x, kTcRows);
+                if (r == 0) mbar_arrive(smem_addr(&p_full[x]));
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            tc_named_sync(1, kTcSoftmax);
-            if (ts == 0) mbar_arrive(smem_addr(&p_full[0]));
-        }
-        // epilogue: O / l for the row (both halves' sums), in q's dtype
-        xm[ts] = l;
-        tc_named_sync(1, kTcSoftmax);
-        const float lt = l + xm[(1 - hf) * kTcRows + r];
-        if (ok) ok = __all_sync(kFull, wait(&o_done[0], (nch - 1) & 1, 0x1000u));
-        if (ok) {
-            tc_fence_after();
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            uint16_t* dst = static_cast<uint16_t*>(p.out) +
-                            ((long long)(cu + qi) * p.hq + kvh * G + r % G) * D + hf * (D / 2);
+            if (ok) ok = __all_sync(kFull, wait(&o_done[x], (nch - 1) & 1, 0x1000u));
+            if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint16_t* dst = static_cast<uint16_t*>(p.out) + ((long long)(cu + qi) * p.hq + kvh * G + r % G) * D;
 #pragma unroll
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                float o[32];
-                tc_ld32(tm_o + lane_addr + hf * (D / 2) + c0, o);
-                if (rv) {
-                    uint32_t w[16];
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float o[32];
+                    tc_ld32(tm_o + lane_addr + c0, o);
+                    if (rv) {
+                        uint32_t w[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack2<KV>(o[2 * i] * inv, o[2 * i + 1] * inv);
+                        for (int i = 0; i < 16; ++i) w[i] = pack2<KV>(o[2 * i] * inv, o[2 * i + 1] * inv);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
                 }
             }
         }
@@ -1099,11 +1067,14 @@ using TcLaunch = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const M
 template <typename KV, int D, int G>
 cudaError_t tc_launch(const CUtensorMap& k, const CUtensorMap& v, const MqParams& p, int grid,
                       cudaStream_t st) {
+    // two row tiles per CTA: grid counts tile pairs
     const int smem = TcCfg<D>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(mq_tc_kernel<KV, D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(mq_tc_kernel<KV, D, G>, dim3(grid), dim3(kTcThreads), size_t(smem), st, k, v, p);
+    const long long tiles = (long long)grid / p.tmax;
+    const int g2 = int(tiles * ((p.tmax + 1) / 2));
+    return launch_pdl(mq_tc_kernel<KV, D, G>, dim3(g2), dim3(kTcThreads), size_t(smem), st, k, v, p);
 }
 template <typename KV, int D>
 TcLaunch tc_pick_g(int G) {
