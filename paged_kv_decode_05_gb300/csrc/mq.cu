@@ -791,6 +791,7 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             float m = -INFINITY, l = 0.f;
             unsigned char* ph = smem + C::OFF_P + x * 2 * C::PBYTES + r * 128;
             const int last_blk_tok = ((L - 1) / kBlockSize) * kBlockSize;
+            const bool qpos = p.qscale > 0.f;                  // max of raw scores = max of scaled
             bool ok = true;
             for (int c = 0; c < nch; ++c) {
                 const int st = c % kTcStages;
@@ -800,17 +801,27 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                 float s[kTcChunk];
                 float mx = -INFINITY;
                 int mask = 0;
+                bool plain = false;   // warp-uniform: raw scores, every column visible
                 if (ok) {
                     tc_fence_after();
                     tc_ld32(tm_s + lane_addr + (c & 1) * kTcChunk, s);
                     tc_ld32(tm_s + lane_addr + (c & 1) * kTcChunk + 32, s + 32);
                     mask = smask[st];
+                    plain = __all_sync(kFull, rv && pos - tok0 >= kTcChunk - 1 &&
+                                                  mask == (1 << (kTcChunk / kBlockSize)) - 1) && qpos;
+                    if (plain) {
+                        float mr = s[0];
 #pragma unroll
-                    for (int i = 0; i < kTcChunk; ++i) {
-                        const int tok = tok0 + i;
-                        const bool vis = rv && tok <= pos && ((mask >> (i / kBlockSize)) & 1);
-                        s[i] = vis ? s[i] * p.qscale : -INFINITY;
-                        mx = fmaxf(mx, s[i]);
+                        for (int i = 1; i < kTcChunk; ++i) mr = fmaxf(mr, s[i]);
+                        mx = mr * p.qscale;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kTcChunk; ++i) {
+                            const int tok = tok0 + i;
+                            const bool vis = rv && tok <= pos && ((mask >> (i / kBlockSize)) & 1);
+                            s[i] = vis ? s[i] * p.qscale : -INFINITY;
+                            mx = fmaxf(mx, s[i]);
+                        }
                     }
                     if (c > 0) ok = __all_sync(kFull, wait(&o_done[x], (c - 1) & 1, 0x1000u));
                 }
@@ -830,22 +841,30 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                         if (grow && m > -INFINITY) l *= a;
                     }
                     if (grow) m = mx;
+                    // P = exp2(s - m) as hi + lo 16-bit parts, written swizzled (row r)
+                    auto emit = [&](auto expo) {
 #pragma unroll
-                    for (int c16 = 0; c16 < kTcChunk / 8; ++c16) {
-                        uint32_t hw[4], lw[4];
+                        for (int c16 = 0; c16 < kTcChunk / 8; ++c16) {
+                            uint32_t hw[4], lw[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float y0 = s[c16 * 8 + 2 * e], y1 = s[c16 * 8 + 2 * e + 1];
-                            const float x0 = y0 == -INFINITY ? 0.f : fast_exp2(y0 - m);
-                            const float x1 = y1 == -INFINITY ? 0.f : fast_exp2(y1 - m);
-                            l += x0 + x1;
-                            hw[e] = pack2<KV>(x0, x1);
-                            const float2 rr = unpack2(KV{}, hw[e]);
-                            lw[e] = pack2<KV>(x0 - rr.x, x1 - rr.y);
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = expo(s[c16 * 8 + 2 * e]);
+                                const float x1 = expo(s[c16 * 8 + 2 * e + 1]);
+                                l += x0 + x1;
+                                hw[e] = pack2<KV>(x0, x1);
+                                const float2 rr = unpack2(KV{}, hw[e]);
+                                lw[e] = pack2<KV>(x0 - rr.x, x1 - rr.y);
+                            }
+                            const uint32_t off = uint32_t((c16 ^ (r & 7)) << 4);
+                            *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            *reinterpret_cast<uint4*>(ph + C::PBYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                         }
-                        const uint32_t off = uint32_t((c16 ^ (r & 7)) << 4);
-                        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(ph + C::PBYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    };
+                    if (plain) {   // finite raw scores, m finite: one fma and one ex2 each
+                        const float nm = -m, qs = p.qscale;
+                        emit([&](float y) { return fast_exp2(fmaf(y, qs, nm)); });
+                    } else {
+                        emit([&](float y) { return y == -INFINITY ? 0.f : fast_exp2(y - m); });
                     }
                     // tile 0 zeroes V rows past the context (both tiles' P.V
                     // follow tile 0's P in the MMA thread's order)
