@@ -149,6 +149,36 @@ def test_tensor_core_row_tiles(name):
     assert int(g.status.item()) == 0
 
 
+@pytest.mark.parametrize("name", ["spec_verify", "prefill_chunk"])   # mma.sync / tcgen05 kernel
+def test_bad_block_entry_and_length_are_flagged(name):
+    """An out-of-pool table entry and a length beyond the table are flagged on
+    the status word; the over-long sequence's rows are not written and the
+    other sequences stay exact."""
+    import torch
+    from paged_kv_decode_05_gb300 import binding as B
+    w, g, o, want = case(name)
+    bt = g.block_tables.clone()
+    bt[0, 1] = w.num_blocks + 7                       # outside the pool
+    lens = g.context_lens.clone()
+    lens[1] = bt.shape[1] * 16 + 64                   # longer than the table
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qd = to_dev(w.q)
+    out = torch.full(qd.shape, float("nan"), dtype=qd.dtype, device="cuda")
+    cu = to_dev(np.asarray(w.cu_q, np.int32))
+    ws = torch.empty(B.pkv_multiquery_workspace_size(w.cfg.batch, w.cfg.num_q_heads, w.cfg.q_len,
+                                                     g.k_cache, 0), dtype=torch.uint8, device="cuda")
+    B.pkv_multiquery_attn(qd, cu, w.cfg.q_len, g.k_cache, g.v_cache, bt, lens,
+                          w.cfg.softmax_scale, out, ws, 0, status)
+    _sync()
+    st = int(status.item())
+    assert st & B.DEV_BAD_BLOCK and st & B.DEV_BAD_LENGTH
+    got = out_to_f64(out)
+    rows = lambda b: np.arange(w.cu_q[b], w.cu_q[b + 1])   # noqa: E731
+    assert np.isnan(got[rows(1)]).all()               # not written
+    keep = np.concatenate([rows(b) for b in range(2, w.cfg.batch)])
+    assert_attention_close(got[keep], want[keep], False, f"{name} other sequences")
+
+
 def test_too_many_queries_are_flagged_not_written():
     import torch
     from paged_kv_decode_05_gb300 import binding as B
