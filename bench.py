@@ -98,13 +98,14 @@ def recorded_traffic(kernel: str, config: str):
 
     profiles/<kernel>_<config>.md carries a line
     ``traffic_bytes_per_launch: N source_sha256: H``; it counts only while H
-    matches the current kernel source.
+    matches the current kernel source (decode.cu followed by common.cuh).
     """
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
-    src = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc", "decode.cu")
+    csrc = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc")
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        body = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("decode.cu", "common.cuh"))
+        h = hashlib.sha256(body).hexdigest()[:16]
         for line in open(path):
             if line.startswith("traffic_bytes_per_launch:"):
                 parts = line.split()

@@ -36,15 +36,12 @@ __device__ __forceinline__ float2 unpack2(F16, uint32_t w) {
     __half2 h = *reinterpret_cast<__half2*>(&w);
     return __half22float2(h);
 }
-// Two int8 codes (selected bytes of a word already XOR-ed with 0x80808080,
-// i.e. biased to x + 128) -> fp16x2 holding the codes exactly: the byte
-// becomes the low mantissa byte of 1024 (fp16 0x6400), then 1152 is
-// subtracted. `sel` picks the bytes: 0x4140 -> bytes 0,1; 0x4342 -> bytes 2,3.
-__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t biased, uint32_t sel) {
-    const uint32_t h = __byte_perm(biased, 0x64646464u, sel);
-    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h),
-                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
-    return *reinterpret_cast<const uint32_t*>(&v);
+// Two int8 codes c (selected bytes of a word already XOR-ed with 0x80808080,
+// i.e. c + 128) -> fp16x2 holding 1152 + c exactly: the byte becomes the low
+// mantissa byte of 1024 (fp16 0x6400). The caller removes the 1152 bias.
+// `sel` picks the bytes: 0x4140 -> bytes 0,1; 0x4342 -> bytes 2,3.
+__device__ __forceinline__ uint32_t i8x2_biased_h2(uint32_t biased, uint32_t sel) {
+    return __byte_perm(biased, 0x64646464u, sel);
 }
 
 // d += a * b on the tensor cores: m16n8k16, fp16 inputs, fp32 accumulators

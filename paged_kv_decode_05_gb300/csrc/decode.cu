@@ -301,9 +301,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     //  * O^T[dims x heads] += V^T[dims x 16 tokens] P^T[16 tokens x heads]: lane
     //    (gq, tq) accumulates dims [gq*D/8, (gq+1)*D/8) of heads 2tq, 2tq + 1,
     //    so its softmax state is that of its own two heads.
-    // 16-bit caches multiply in their own type; INT8 codes become fp16 exactly
-    // (the biased byte as the low mantissa byte of 1024, then one packed
-    // subtraction), q is rounded to fp16 and the block's V scale rides on P.
+    // 16-bit caches multiply in their own type. INT8 codes c enter as the
+    // fp16 value 1152 + c, exact (the byte c + 128 as the low mantissa byte of
+    // 1024): the bias adds 1152 * sum_d q_d to every score of a head, taken
+    // off before the block's K scale, and 1152 * sum_t P_t to every O entry
+    // of a head, taken off when the piece is written (sum_t P_t kept beside
+    // O with the same rescalings). q is rounded to fp16 and the block's V
+    // scale rides on P.
     using MMT = typename std::conditional<C::kI8, F16, KV>::type;   // mma operand type
     constexpr int MT = D / 16;                   // m-tiles of P.V
     constexpr int DL = D / 8;                    // dims a lane row group owns
@@ -317,21 +321,32 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     // toward the fp16 limit) and multiplied back when the piece is written.
     int vexp = 0;
     float vmul = 1.f;                            // 2^-vexp
+    float kbias[2] = {0.f, 0.f};                 // INT8: 1152 * sum_d q_d, heads 2tq + e
+    float pv[2] = {0.f, 0.f};                    // INT8: sum_t P_t of this lane's tokens
 
     auto finalize = [&]() {
         const int nbk = prefix[pb + 1] - prefix[pb];
         const long long seg = (long long)pb * p.hkv + pkvh;
         const bool whole = (first_j == 0 && last_j == nbk - 1);
         float lh[2] = {lsum[0], lsum[1]};
+        float ph[2] = {pv[0], pv[1]};
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) lh[e] += __shfl_xor_sync(kFull, lh[e], off);
+            for (int e = 0; e < 2; ++e) {
+                lh[e] += __shfl_xor_sync(kFull, lh[e], off);
+                if constexpr (C::kI8) ph[e] += __shfl_xor_sync(kFull, ph[e], off);
+            }
         const float up = C::kI8 ? ldexpf(1.f, vexp) : 1.f;   // O back from units of 2^vexp
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int h = 2 * tq + e;
             if (h >= G) continue;
+            if constexpr (C::kI8) {   // the V bias: O -= 1152 * sum_t P_t
+                const float cb = 1152.f * ph[e];
+#pragma unroll
+                for (int i = 0; i < MT; ++i) { oa[i][e] -= cb; oa[i][2 + e] -= cb; }
+            }
             if (whole) {
                 float2 v[MT];
 #pragma unroll
@@ -389,20 +404,21 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
             }
         } else {
             // INT8: DL codes per row; the bytes of two tokens are interleaved,
-            // then each pair becomes fp16x2 exactly
+            // then each pair becomes the fp16x2 (1152 + c0, 1152 + c1). Rows
+            // past the context need no zeroing: any byte is a finite code and
+            // its P is exactly 0.
+            (void)nv;
             uint32_t vw[4][DL / 4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
                 const unsigned char* row = vt + t * C::ROW + gq * DL;
-                const bool keep = t < nv;
                 if constexpr (DL == 16) {
                     const uint4 x = *reinterpret_cast<const uint4*>(row);
-                    vw[i][0] = keep ? x.x : 0u; vw[i][1] = keep ? x.y : 0u;
-                    vw[i][2] = keep ? x.z : 0u; vw[i][3] = keep ? x.w : 0u;
+                    vw[i][0] = x.x; vw[i][1] = x.y; vw[i][2] = x.z; vw[i][3] = x.w;
                 } else {
                     const uint2 x = *reinterpret_cast<const uint2*>(row);
-                    vw[i][0] = keep ? x.x : 0u; vw[i][1] = keep ? x.y : 0u;
+                    vw[i][0] = x.x; vw[i][1] = x.y;
                 }
             }
 #pragma unroll
@@ -413,10 +429,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                     const uint32_t x = __byte_perm(vw[0][k], vw[1][k], sel) ^ 0x80808080u;
                     const uint32_t y = __byte_perm(vw[2][k], vw[3][k], sel) ^ 0x80808080u;
                     const int i = 2 * k + hb;
-                    va[i][0] = i8x2_to_h2(x, 0x4140);
-                    va[i][1] = i8x2_to_h2(x, 0x4342);
-                    va[i][2] = i8x2_to_h2(y, 0x4140);
-                    va[i][3] = i8x2_to_h2(y, 0x4342);
+                    va[i][0] = i8x2_biased_h2(x, 0x4140);
+                    va[i][1] = i8x2_biased_h2(x, 0x4342);
+                    va[i][2] = i8x2_biased_h2(y, 0x4140);
+                    va[i][3] = i8x2_biased_h2(y, 0x4342);
                 }
             }
         }
@@ -472,6 +488,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                         }
                     }
                 }
+            }
+            if constexpr (C::kI8) {
+                // sum of the fp16 q of head gq (the values the MMAs multiply),
+                // over the lane's dims, then over the 4 lanes of the head
+                float qsum = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const float2 a = unpack2(F16{}, qb[kk][0]), b = unpack2(F16{}, qb[kk][1]);
+                    qsum += (a.x + a.y) + (b.x + b.y);
+                }
+                qsum += __shfl_xor_sync(kFull, qsum, 1);
+                qsum += __shfl_xor_sync(kFull, qsum, 2);
+#pragma unroll
+                for (int e = 0; e < 2; ++e)   // head 2tq + e lives in lanes 4(2tq + e) + [0, 4)
+                    kbias[e] = 1152.f * __shfl_sync(kFull, qsum, (8 * tq + 4 * e) & 31);
+                pv[0] = pv[1] = 0.f;
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) { m[e] = -INFINITY; lsum[e] = 0.f; }
@@ -541,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                     for (int i = 0; i < MT; ++i) {
                         oa[i][0] *= r; oa[i][1] *= r; oa[i][2] *= r; oa[i][3] *= r;
                     }
+                    pv[0] *= r; pv[1] *= r;
                     vexp = nexp;
                     vmul = ldexpf(1.f, -nexp);
                 }
@@ -565,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t u0 = w0[kk] ^ 0x80808080u, u1 = w1[kk] ^ 0x80808080u;
-                    mma_16816_f16(acc[kk & 1], i8x2_to_h2(u0, 0x4140), i8x2_to_h2(u1, 0x4140),
-                                  i8x2_to_h2(u0, 0x4342), i8x2_to_h2(u1, 0x4342),
+                    mma_16816_f16(acc[kk & 1], i8x2_biased_h2(u0, 0x4140), i8x2_biased_h2(u1, 0x4140),
+                                  i8x2_biased_h2(u0, 0x4342), i8x2_biased_h2(u1, 0x4342),
                                   qb[kk][0], qb[kk][1]);
                 }
             }
@@ -575,8 +608,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const bool hv = 2 * tq + e < G;
-                sv[0][e] = (hv && gq < nv) ? (acc[0][e] + acc[1][e]) * sk : -INFINITY;
-                sv[1][e] = (hv && gq + 8 < nv) ? (acc[0][2 + e] + acc[1][2 + e]) * sk : -INFINITY;
+                float s0 = acc[0][e] + acc[1][e], s1 = acc[0][2 + e] + acc[1][2 + e];
+                if constexpr (C::kI8) {   // the K bias comes off before the scale
+                    s0 -= kbias[e];
+                    s1 -= kbias[e];
+                }
+                sv[0][e] = (hv && gq < nv) ? s0 * sk : -INFINITY;
+                sv[1][e] = (hv && gq + 8 < nv) ? s1 * sk : -INFINITY;
             }
             float alpha[2];
 #pragma unroll
@@ -590,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                 const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mn);
                 const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mn);
                 lsum[e] = lsum[e] * alpha[e] + p0 + p1;
+                if constexpr (C::kI8) pv[e] = fmaf(pv[e], alpha[e], (p0 + p1) * vsc);
                 if (2 * tq + e < G) {   // P[head][token], times the block's V scale
                     pbuf[(2 * tq + e) * kBlockSize + gq] = p0 * vsc;
                     pbuf[(2 * tq + e) * kBlockSize + gq + 8] = p1 * vsc;
