@@ -93,18 +93,18 @@ def load_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def recorded_traffic(kernel: str, config: str):
+def recorded_traffic(kernel: str, config: str, source: str = "decode.cu"):
     """DRAM bytes per launch from the committed ncu summary, if still current.
 
     profiles/<kernel>_<config>.md carries a line
     ``traffic_bytes_per_launch: N source_sha256: H``; it counts only while H
-    matches the current kernel source (decode.cu followed by common.cuh).
+    matches the current kernel source (``source`` followed by common.cuh).
     """
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
     csrc = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc")
     try:
-        body = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("decode.cu", "common.cuh"))
+        body = b"".join(open(os.path.join(csrc, f), "rb").read() for f in (source, "common.cuh"))
         h = hashlib.sha256(body).hexdigest()[:16]
         for line in open(path):
             if line.startswith("traffic_bytes_per_launch:"):
@@ -641,11 +641,22 @@ def run_multiquery(args):
     evs = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
            for i in range(0, args.steps, max(1, args.event_every))}
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(str(getattr(props, "uuid", 0)).strip())
+    if str(sampler.gpu_id) and not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + sampler.gpu_id
+    sampler.start()
+    time.sleep(0.5)
+    torch.cuda.synchronize(device)
+    wall0 = time.time()
     a.record()
     for i in range(args.steps):
         step(evs.get(i))
     b.record()
     torch.cuda.synchronize(device)
+    wall1 = time.time()
+    time.sleep(0.2)
+    clocks = sampler.stop(wall0, wall1)
     ms = a.elapsed_time(b) / args.steps
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs.values()) / len(evs)
     alg = algorithmic_bytes(cfg, w.context_lens)
@@ -657,19 +668,28 @@ def run_multiquery(args):
     tpeak, tsrc = load_tensor_peak()
     gbs = alg / (attn_ms / 1e3) / 1e9
     tflops = flops / (attn_ms / 1e3) / 1e12
+    # The library's dispatch rule: runs that fill 128-row tiles (q_len x the
+    # group size) take the tcgen05 kernel, one launch; shorter runs the
+    # mma.sync split kernel and its combine, two launches. Plus the append.
+    g = cfg.num_q_heads // cfg.num_kv_heads
+    tc = nq * g >= 128
+    kernel = "mq_tc_kernel" if tc else "mq_split_kernel"
+    launches = 2 if tc else 3
+    traffic = recorded_traffic(kernel, args.config, "mq.cu")
     # Bound: the workload's FLOP/byte against the machine balance (measured
     # tensor peak / measured HBM bandwidth). Long prefill chunks are dense
     # contractions; verification of a few draft tokens streams the cache.
     if flops / alg > tpeak * 1e12 / (peak * 1e9):
-        roof = {"kernel": "mq_split_kernel", "bound": "tensor", "achieved": round(tflops, 1),
+        roof = {"kernel": kernel, "bound": "tensor", "achieved": round(tflops, 1),
                 "peak": tpeak, "peak_source": tsrc, "unit": "TFLOP/s",
-                "frac": round(tflops / tpeak, 4), "traffic": None,
-                "note": "mma.sync m16n8k16 (bf16 in, fp32 accumulate) against the dense "
-                        "bf16 GEMM peak"}
+                "frac": round(tflops / tpeak, 4), "traffic": traffic,
+                "note": ("tcgen05.mma (bf16 in, fp32 accumulate in TMEM)" if tc else
+                         "mma.sync m16n8k16 (bf16 in, fp32 accumulate)") +
+                        " against the dense bf16 GEMM peak"}
     else:
-        roof = {"kernel": "mq_split_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+        roof = {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1),
                 "peak": peak, "peak_source": src_name, "unit": "GB/s",
-                "frac": round(gbs / peak, 4), "traffic": None}
+                "frac": round(gbs / peak, 4), "traffic": traffic}
     print(json.dumps({
         "metric": "multi-query paged attention HBM GB/s (causal, q_len new tokens/sequence)",
         "value": round(alg / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
@@ -680,8 +700,9 @@ def run_multiquery(args):
         "attn_ms_avg": round(attn_ms, 6), "attn_tflops": round(tflops, 1),
         "query_tokens_per_s": round(cfg.batch * nq / (ms / 1e3), 1),
         "roofline": roof,
+        "clocks": clocks,
         "device_status": int(st["status"].item()),
-        "gpu_launches": args.steps * 3}), flush=True)
+        "gpu_launches": args.steps * launches}), flush=True)
 
 
 def main(argv=None):

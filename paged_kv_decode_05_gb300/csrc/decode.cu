@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
             // of a 128-byte span in the other order, which spreads each quarter
             // warp over all 32 banks, and the groups are put back in registers.
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const bool kswap = (gq & 1) != 0;
+            const bool kswap = !C::kI8 && (gq & 1) != 0;
             if constexpr (!C::kI8) {
                 if (flags & 4) {   // fused step: the new token's row goes to the cache
                     const int r = (mt.w - 1) % kBlockSize;
