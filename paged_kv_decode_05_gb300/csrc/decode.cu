@@ -371,6 +371,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     // Tokens at or past `nv` are zeroed (stale rows may hold anything, and
     // 0 * NaN would poison the sum).
     uint32_t va[MT][4];
+    // INT8: the V codes of the lane's four rows, read before the softmax (its
+    // P stores would otherwise order these shared-memory reads after them)
+    uint32_t vw8[4][C::kI8 ? DL / 4 : 1];
+    auto read_v8 = [&](const unsigned char* vt) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
+            const unsigned char* row = vt + t * C::ROW + gq * DL;
+            if constexpr (DL == 16) {
+                const uint4 x = *reinterpret_cast<const uint4*>(row);
+                vw8[i][0] = x.x; vw8[i][1] = x.y; vw8[i][2] = x.z; vw8[i][3] = x.w;
+            } else if constexpr (DL == 8) {
+                const uint2 x = *reinterpret_cast<const uint2*>(row);
+                vw8[i][0] = x.x; vw8[i][1] = x.y;
+            }
+        }
+    };
     auto load_v = [&](const unsigned char* vt, int nv) {
         if constexpr (!C::kI8) {
             // 16-bit: a lane reads DL dims of each of its four rows; lanes of
@@ -403,24 +420,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                 va[i][3] = __byte_perm(vw[2][i], vw[3][i], 0x7632);
             }
         } else {
-            // INT8: DL codes per row; the bytes of two tokens are interleaved,
-            // then each pair becomes the fp16x2 (1152 + c0, 1152 + c1). Rows
-            // past the context need no zeroing: any byte is a finite code and
-            // its P is exactly 0.
+            // INT8: DL codes per row (read by read_v8); the bytes of two
+            // tokens are interleaved, then each pair becomes the fp16x2
+            // (1152 + c0, 1152 + c1). Rows past the context need no zeroing:
+            // any byte is a finite code and its P is exactly 0.
+            (void)vt;
             (void)nv;
-            uint32_t vw[4][DL / 4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
-                const unsigned char* row = vt + t * C::ROW + gq * DL;
-                if constexpr (DL == 16) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(row);
-                    vw[i][0] = x.x; vw[i][1] = x.y; vw[i][2] = x.z; vw[i][3] = x.w;
-                } else {
-                    const uint2 x = *reinterpret_cast<const uint2*>(row);
-                    vw[i][0] = x.x; vw[i][1] = x.y;
-                }
-            }
+            auto& vw = vw8;
 #pragma unroll
             for (int k = 0; k < DL / 4; ++k) {
 #pragma unroll
@@ -602,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                                   i8x2_biased_h2(u0, 0x4342), i8x2_biased_h2(u1, 0x4342),
                                   qb[kk][0], qb[kk][1]);
                 }
+                read_v8(vt);
             }
             const float sk = p.qscale * ksc;
             float sv[2][2];   // [token gq / gq + 8][head 2tq + e]
