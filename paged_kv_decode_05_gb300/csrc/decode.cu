@@ -371,8 +371,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     // Tokens at or past `nv` are zeroed (stale rows may hold anything, and
     // 0 * NaN would poison the sum).
     uint32_t va[MT][4];
-    // INT8: the V codes of the lane's four rows, read before the softmax (its
-    // P stores would otherwise order these shared-memory reads after them)
+    // The V data of the lane's four rows, read before the softmax (its P
+    // stores would otherwise order these shared-memory reads after them).
+    // 16-bit: lanes of odd tq read a row's two 16-byte chunks in the other
+    // order (halves the bank conflicts of rows that share the bank mapping).
+    uint4 vx16[4][C::kI8 ? 1 : DL / 8];
+    auto read_v16 = [&](const unsigned char* vt) {
+        const int vswap = (DL / 8 == 2) ? (tq & 1) : 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
+            const unsigned char* row = vt + t * C::ROW + gq * DL * 2;
+#pragma unroll
+            for (int c = 0; c < DL / 8; ++c)
+                vx16[i][c] = *reinterpret_cast<const uint4*>(row + 16 * (c ^ vswap));
+        }
+    };
     uint32_t vw8[4][C::kI8 ? DL / 4 : 1];
     auto read_v8 = [&](const unsigned char* vt) {
 #pragma unroll
@@ -390,19 +404,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     };
     auto load_v = [&](const unsigned char* vt, int nv) {
         if constexpr (!C::kI8) {
-            // 16-bit: a lane reads DL dims of each of its four rows; lanes of
-            // odd tq read a row's two 16-byte chunks in the other order (halves
-            // the bank conflicts of rows that share the bank mapping)
+            // 16-bit: DL dims of each of the lane's four rows (read by read_v16)
+            (void)vt;
             uint32_t vw[4][DL / 2];
             const int vswap = (DL / 8 == 2) ? (tq & 1) : 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
-                const unsigned char* row = vt + t * C::ROW + gq * DL * 2;
-                uint4 x[DL / 8];
-#pragma unroll
-                for (int c = 0; c < DL / 8; ++c)
-                    x[c] = *reinterpret_cast<const uint4*>(row + 16 * (c ^ vswap));
+                const uint4* x = vx16[i];
                 const bool keep = t < nv;
 #pragma unroll
                 for (int c = 0; c < DL / 8; ++c) {
@@ -566,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                         mma16816<KV>(acc[1], a1, qb[2 * c + 1][0], qb[2 * c + 1][1]);
                     }
                 }
+                read_v16(vt);
             } else {
                 const float2 sc = scl[s];
                 ksc = sc.x;
