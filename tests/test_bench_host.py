@@ -1,0 +1,108 @@
+"""Host-side logic of bench.py, on the CPU: the ncu traffic record keyed by
+the kernel source, the clock-sample parser, the roofline denominators and
+the default timing arguments."""
+import hashlib
+import json
+import os
+import types
+
+import pytest
+
+import bench
+
+
+def _fake_tree(tmp_path, source="decode.cu", body=b"kernel v1"):
+    csrc = tmp_path / "paged_kv_decode_05_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / source).write_bytes(body)
+    (csrc / "common.cuh").write_bytes(b"helpers")
+    (tmp_path / "profiles").mkdir()
+    return csrc, hashlib.sha256(body + b"helpers").hexdigest()[:16]
+
+
+def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    csrc, h = _fake_tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    prof = tmp_path / "profiles" / "decode_split_kernel_gqa8b.md"
+    prof.write_text(f"# summary\n\ntraffic_bytes_per_launch: 12345 source_sha256: {h}\n")
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") == 12345
+    # another workload has no summary
+    assert bench.recorded_traffic("decode_split_kernel", "mha7b") is None
+    # the kernel changed since the capture: the figure no longer counts
+    (csrc / "decode.cu").write_bytes(b"kernel v2")
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") is None
+    # so does a change to the shared header
+    (csrc / "decode.cu").write_bytes(b"kernel v1")
+    (csrc / "common.cuh").write_bytes(b"helpers v2")
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") is None
+
+
+def test_recorded_traffic_for_the_multiquery_source(tmp_path, monkeypatch):
+    _, h = _fake_tree(tmp_path, source="mq.cu", body=b"mq kernels")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    prof = tmp_path / "profiles" / "mq_tc_kernel_prefill_chunk.md"
+    prof.write_text(f"traffic_bytes_per_launch: 777 source_sha256: {h}\n")
+    assert bench.recorded_traffic("mq_tc_kernel", "prefill_chunk", "mq.cu") == 777
+    # keyed on decode.cu it does not match (and decode.cu is absent here)
+    assert bench.recorded_traffic("mq_tc_kernel", "prefill_chunk") is None
+
+
+class _Proc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler(lines):
+    s = bench.ClockSampler("GPU-0")
+    s.proc = _Proc()
+    s.thread = types.SimpleNamespace(join=lambda timeout=None: None)
+    s.lines = lines
+    return s
+
+
+def test_clock_sampler_keeps_the_timed_window_and_reasons():
+    lines = [
+        (0.5, "1000, 2070, 300.0, Not Active, Not Active, Not Active, Not Active"),   # before
+        (1.0, "2070, 2070, 900.5, Not Active, Not Active, Not Active, Not Active"),
+        (1.1, "2055, 2070, 950.0, Not Active, Not Active, Not Active, Active"),
+        (1.2, "2070, 2070, 940.0, Not Active, Not Active, Not Active, Not Active"),
+        (1.3, "[N/A], 2070, 940.0, Not Active, Not Active, Not Active, Not Active"),  # unparsable
+        (1.4, "2070, 2070"),                                                         # short line
+        (9.0, "500, 2070, 100.0, Active, Not Active, Not Active, Not Active"),         # after
+    ]
+    c = _sampler(lines).stop(1.0, 2.0)
+    assert c["samples"] == 3
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]   # the hw_slowdown sample lies outside the window
+
+
+def test_clock_sampler_without_nvidia_smi():
+    s = bench.ClockSampler("GPU-0")
+    c = s.stop(0.0, 1.0)
+    assert c["sm_mhz"] is None and c["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_peaks_measured_or_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
+    assert bench.load_tensor_peak() == (bench.FALLBACK_BF16_TFLOPS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6794.8, "bf16_tflops": 1919.9}))
+    assert bench.load_peaks() == (6794.8, "measured")
+    assert bench.load_tensor_peak() == (1919.9, "measured")
+
+
+def test_default_timing_arguments():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1
+    assert a.impl != "reference" and a.config == "gqa8b"
+    b = bench.parse_args(["--impl", "reference", "--steps", "5", "--warmup", "3"])
+    assert b.impl == "reference" and b.steps == 5 and b.warmup == 3
+
+
+@pytest.mark.parametrize("argv", [["--config", "nope"], ["--op", "nope"]])
+def test_unknown_choices_are_rejected(argv):
+    with pytest.raises(SystemExit):
+        bench.parse_args(argv)
