@@ -138,7 +138,7 @@ pkv_status pkv_append(const void *k_new, const void *v_new, pkv_dtype src_dtype,
  * pkv_decode_workspace_size, pkv_decode_split and pkv_decode_combine.
  *
  * Supported: block_size 16, head_dim 64 or 128, num_q_heads/num_kv_heads in
- * {1, 2, 4}, 1 <= batch <= 8192; q_dtype == kv_dtype for fp16/bf16 caches,
+ * {1, 2, 4, 8}, 1 <= batch <= 8192; q_dtype == kv_dtype for fp16/bf16 caches,
  * q_dtype PKV_F16 or PKV_BF16 for INT8 caches. q, out, caches 16-byte aligned;
  * workspace 256-byte aligned.
  * ------------------------------------------------------------------------ */

@@ -20,11 +20,13 @@
 //   scales follow by cp.async on the same barrier. Block-table entries for the
 //   next 32 units are fetched ahead, one per lane.
 // * All g query heads of a KV head are served by the warp that reads its
-//   tiles, so each tile is read from HBM once. Scores use 8 lanes per token
-//   (q held in registers for the lane's 16 dims), packed fp32x2 FMAs and an
-//   exchange-halving shuffle reduction; the online softmax keeps a running
-//   max and sum per head in the exp2 domain; P.V gives each lane D/32
-//   output dims for all g heads.
+//   tiles, so each tile is read from HBM once. Both contractions run on the
+//   tensor cores (mma.sync m16n8k16, fp32 accumulators): scores as
+//   S[16 tokens x 8 head columns] (g <= 8 heads, padded), P.V as
+//   O^T[dims x heads] += V^T[dims x 16 tokens] P^T, so each lane keeps the
+//   online-softmax state (running max and sum, exp2 domain) of its own two
+//   heads. INT8 codes enter the MMAs as exact fp16 values with a bias that is
+//   taken off per head.
 // * A segment that lies inside one warp's range is normalised and written
 //   out directly. Pieces of a segment that crosses ranges leave (m, l, o) in
 //   the workspace at slot (segment + worker), which is unique because both
@@ -70,7 +72,7 @@ struct Cfg {
     static constexpr int WARP_BYTES = align_up(OFF_Q + NS * QBYTES, 128);
     static_assert(NS >= 2 && NS <= 32, "stage count (one parity bit per stage)");
     static_assert(STAGE % 128 == 0 && OFF_Q % 128 == 0 && QBYTES % 16 == 0, "copy alignment");
-    static_assert(G == 1 || G == 2 || G == 4, "group size");
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size (heads fill <= 8 MMA columns)");
 };
 
 // Dynamic shared memory starts with 4 ints of scan scratch, then the block
@@ -831,6 +833,7 @@ bool pick_g(int G, Ops* o) {
         case 1: *o = Impl<KV, QT, D, 1>::ops(); return true;
         case 2: *o = Impl<KV, QT, D, 2>::ops(); return true;
         case 4: *o = Impl<KV, QT, D, 4>::ops(); return true;
+        case 8: *o = Impl<KV, QT, D, 8>::ops(); return true;
     }
     return false;
 }

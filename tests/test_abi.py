@@ -88,7 +88,7 @@ def _decode(lib, fn, q_dtype=B.PKV_BF16, d=None, batch=4, hq=8, ws=None, ws_byte
 def test_decode_host_validation(lib):
     for fn in ("pkv_decode_attn", "pkv_decode_split"):
         assert _decode(lib, fn, hq=7) == 1                       # hq % hkv
-        assert _decode(lib, fn, hq=16) == 2                      # group 8 not built
+        assert _decode(lib, fn, hq=32) == 2                      # group 16 not built
         assert _decode(lib, fn, d=desc(d=80)) == 2
         assert _decode(lib, fn, d=desc(bs=32)) == 2
         assert _decode(lib, fn, q_dtype=B.PKV_F16) == 1          # q != kv 16-bit type
@@ -110,6 +110,10 @@ def test_workspace_size_formula(lib):
     a = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert got == a(4 * 257) + a(slots * 4 * 2 * 4) + a(slots * 4 * 128 * 4)
     assert lib.pkv_decode_workspace_size(256, 12, ctypes.byref(d), 64) == 0  # unsupported group
+    assert lib.pkv_decode_workspace_size(256, 128, ctypes.byref(d), 64) == 0  # group 16
+    g8 = lib.pkv_decode_workspace_size(256, 64, ctypes.byref(d), 1216)        # group 8
+    slots = 256 * 8 + 1216
+    assert g8 == a(4 * 257) + a(slots * 8 * 2 * 4) + a(slots * 8 * 128 * 4)
 
 
 def test_multiquery_and_copy_blocks_host_validation(lib):

@@ -41,6 +41,14 @@ SMALL = {
                           len_groups=((7, 1, 400),)),
     "f16_d128_g4": variant(CONFIGS["gqa8b"], batch=9, kv_dtype="f16", q_dtype="f16",
                            src_dtype="f16", len_groups=((9, 1, 500),)),
+    # group 8: eight query heads per KV head (64 q / 8 kv heads, the 70B-class shape)
+    "bf16_d128_g8": variant(CONFIGS["gqa8b"], batch=8, num_q_heads=64, num_kv_heads=8,
+                            len_groups=((8, 1, 900),)),
+    "i8_d128_g8": variant(CONFIGS["gqa8b_int8"], batch=6, num_q_heads=64, num_kv_heads=8,
+                          len_groups=((6, 1, 600),)),
+    "f16_d64_g8": variant(CONFIGS["gqa8b"], batch=7, num_q_heads=16, num_kv_heads=2,
+                          head_dim=64, kv_dtype="f16", q_dtype="f16", src_dtype="f16",
+                          len_groups=((7, 1, 500),)),
 }
 
 _cache = {}

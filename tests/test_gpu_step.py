@@ -22,6 +22,8 @@ def built():
                        len_groups=((3, 3000, 9000), (9, 16, 256)))),
     ("tiny", CONFIGS["tiny"]),
     ("mha_d128", variant(CONFIGS["mha7b"], batch=5, len_groups=((5, 1, 600),))),
+    ("g8_d128", variant(CONFIGS["gqa8b"], batch=6, num_q_heads=64, num_kv_heads=8,
+                        len_groups=((6, 0, 700),))),
     # the new token in row 0 (no cache rows copied), row 15, and L = 0
     ("edges", variant(CONFIGS["gqa8b"], batch=14, len_groups=(
         (2, 0, 0), (2, 1, 1), (2, 16, 16), (2, 17, 17), (2, 31, 31), (2, 32, 32), (2, 33, 33)))),
