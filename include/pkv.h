@@ -129,8 +129,8 @@ pkv_status pkv_append(const void *k_new, const void *v_new, pkv_dtype src_dtype,
  * is rounded to q's dtype (nearest-even).
  *
  * Work split: the (sequence, kv_head, block) units of the whole batch are cut
- * into num_parts equal contiguous ranges, one per worker warp (0 = one worker
- * per resident warp slot of the device). A sequence whose blocks fall in one
+ * into num_parts equal contiguous ranges, one per worker warp (0 = the
+ * device default of pkv_decode_default_parts). A sequence whose blocks fall in one
  * range is finished by that worker; the others leave fp32 partial states in
  * the workspace that the combine step merges:
  *   out = sum_i exp(m_i - M) o_i / sum_i exp(m_i - M) l_i,  M = max_i m_i.
@@ -143,8 +143,10 @@ pkv_status pkv_append(const void *k_new, const void *v_new, pkv_dtype src_dtype,
  * workspace 256-byte aligned.
  * ------------------------------------------------------------------------ */
 
-/* Resident worker warps of the split kernel on `device` (the default
- * num_parts), or 0 if the configuration is unsupported. */
+/* The default num_parts on `device`: the split kernel's resident worker
+ * warps, capped at 2 CTAs (8 warps) per SM for fp16/bf16 caches at head_dim
+ * 128, where fewer, longer workers read the cache faster. 0 if the
+ * configuration is unsupported. */
 int32_t pkv_decode_default_parts(int32_t device, int32_t batch, int32_t num_q_heads,
                                  const pkv_cache_desc *cache);
 

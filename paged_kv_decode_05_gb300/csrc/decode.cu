@@ -800,6 +800,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
 // ------------------------------------------------------------------- host ---
 struct Ops {
     int warp_bytes;
+    int max_ctas_per_sm;   // cap on the default worker count (0 = occupancy)
     cudaError_t (*prepare)(size_t smem);                        // smem attribute
     cudaError_t (*occupancy)(int* blocks, size_t smem);
     void (*split)(const DecodeParams&, int grid, size_t smem, cudaStream_t);
@@ -824,7 +825,14 @@ struct Impl {
     static void combine(const CombineParams& c, int grid, cudaStream_t st) {
         launch_pdl(decode_combine_kernel<QT, D, G>, dim3(grid), dim3(kCombineThreads), 0, st, c);
     }
-    static Ops ops() { return Ops{Cfg<KV, D, G>::WARP_BYTES, prepare, occupancy, split, combine}; }
+    // 16-bit caches at D = 128 default to 2 CTAs (8 worker warps) per SM
+    // although 3 fit: on the GQA-8B workload the split kernel read 6.74 TB/s
+    // with 8 warps per SM against 6.38 TB/s with 12 (same GPU, back to back),
+    // and g = 8, whose shared memory allows only 2, read 6.71 TB/s.
+    static constexpr int kCap = (Elem<KV>::bytes == 2 && D == 128) ? 2 : 0;
+    static Ops ops() {
+        return Ops{Cfg<KV, D, G>::WARP_BYTES, kCap, prepare, occupancy, split, combine};
+    }
 };
 
 template <typename KV, typename QT, int D>
@@ -892,12 +900,14 @@ size_t split_smem(const Ops& o, int batch) {
     return size_t(prefix_bytes(batch)) + size_t(kWarpsPerCta) * o.warp_bytes;
 }
 
-// Resident worker warps on the current device for this configuration.
+// Default worker warps on the current device for this configuration: the
+// resident warps, at most max_ctas_per_sm CTAs per SM.
 long long default_workers(const Ops& o, int batch) {
     int dev = 0, sms = 0, blocks = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (o.occupancy(&blocks, split_smem(o, batch)) != cudaSuccess || blocks <= 0) return 0;
+    if (o.max_ctas_per_sm > 0 && blocks > o.max_ctas_per_sm) blocks = o.max_ctas_per_sm;
     return (long long)sms * blocks * kWarpsPerCta;
 }
 

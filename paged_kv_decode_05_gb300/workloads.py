@@ -24,9 +24,11 @@ Recipe (every config):
   that receive its new tokens are always private (copy-on-write safe). The
   shared prefix is written once.
 
-The five configurations are the shapes of a paged-KV serving loop's decode
-step: a tiny fp16 case, an MHA 7B-shape batch, a Llama-3-8B-shape GQA batch
-(bf16 and INT8 KV) and a skewed long-context mix with shared prefixes.
+The five decode configurations are the shapes of a paged-KV serving loop's
+decode step: a tiny fp16 case, an MHA 7B-shape batch, a Llama-3-8B-shape GQA
+batch (bf16 and INT8 KV) and a skewed long-context mix with shared prefixes.
+Three more cover adjacent work: a 70B-class decode batch with 8 query heads
+per KV head, speculative verification and chunked prefill.
 """
 
 from __future__ import annotations
@@ -98,6 +100,10 @@ CONFIGS = {
         kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
         len_groups=((8, 32768, 131072), (120, 16, 256)), max_len=131072,
         prefix_share=2048),
+    "gqa70b": DecodeConfig(
+        name="gqa70b", batch=256, num_q_heads=64, num_kv_heads=8, head_dim=128,
+        kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
+        len_groups=((256, 128, 4096),), max_len=4096),
     "spec_verify": DecodeConfig(
         name="spec_verify", batch=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
         kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
@@ -116,6 +122,8 @@ DESCRIPTIONS = {
     "gqa8b_int8": "GQA Llama-3-8B-shape INT8 KV: B=256, 32/8 heads, D=128, L~U[128,4096]",
     "skewed": "skewed long-context bf16: 8 x L~U[32768,131072] + 120 x L~U[16,256], "
               "32/8 heads, D=128, 2048-token CoW prefix per 4 sequences",
+    "gqa70b": "GQA 70B-class-shape bf16: B=256, 64 q / 8 kv heads (group 8), D=128, "
+              "L~U[128,4096]",
     "spec_verify": "speculative verification bf16: B=256, 4 draft tokens + 1 per sequence, "
                    "32/8 heads, D=128, L~U[128,4096]",
     "prefill_chunk": "chunked prefill bf16: B=8, 512-token chunk per sequence after a cached "

@@ -13,6 +13,7 @@ SMALL = {
     "gqa8b_int8": variant(CONFIGS["gqa8b_int8"], batch=5, len_groups=((5, 1, 300),)),
     "skewed": variant(CONFIGS["skewed"], batch=10, max_len=9000,
                       len_groups=((3, 3000, 9000), (7, 16, 256))),
+    "gqa70b": variant(CONFIGS["gqa70b"], batch=5, len_groups=((5, 128, 900),)),
     "spec_verify": variant(CONFIGS["spec_verify"], batch=7, len_groups=((7, 5, 600),)),
     "prefill_chunk": variant(CONFIGS["prefill_chunk"], batch=3, q_len=40, max_len=700,
                              len_groups=((3, 40, 700),)),
