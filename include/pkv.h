@@ -32,7 +32,9 @@
  *
  * Ownership and synchronisation: every pointer argument is caller-owned
  * DEVICE memory, except the pkv_cache_desc pointer (host). The library
- * allocates nothing and keeps no state between calls. Every call only
+ * allocates nothing. Between calls it keeps only two lookups, each made once:
+ * the driver's tensor-map encoder (pkv_multiquery_attn) and, per device, the
+ * address of pkv_decode_attn_noalloc's built-in scratch array. Every call only
  * enqueues kernels on `stream` and returns; inputs must stay valid until the
  * stream has executed them.
  *
