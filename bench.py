@@ -405,11 +405,7 @@ def run_native(args):
         "steps": K, "warmup": W, "ms_per_step": round(ms_total / K, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.kv_dtype, "data": "synthetic (seeded N(0,1) K/V/q, shuffled block pool)",
-        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
-                   "batch": cfg.batch, "num_q_heads": cfg.num_q_heads,
-                   "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
-                   "block_size": cfg.block_size, "total_context_tokens": w.total_tokens,
-                   "algorithmic_bytes_per_step": alg, "workers": parts,
+        "config": {**workload_config(args.config, w, alg), "workers": parts,
                    "l2": "no flush: the KV cache read each step (%.2f GB) is far larger than "
                          "the 129 MB L2" % (alg / 1e9),
                    "parallelism": f"replicas x{world}",
@@ -509,6 +505,16 @@ def _e2e(st, w, cfg, ws, parts, device, K, world):
                    "the neighbouring steps' kernels"}
 
 
+def workload_config(name, w, alg):
+    """The keys that identify a decode workload, shared by both arms' lines
+    (algorithmic bytes of one pass over the whole batch: the native arm's step)."""
+    cfg = w.cfg
+    return {"workload": DESCRIPTIONS[name], "name": name, "batch": cfg.batch,
+            "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
+            "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+            "total_context_tokens": w.total_tokens, "algorithmic_bytes_per_batch": alg}
+
+
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is the oracle's decode of
     one sequence of the workload (cycling through the batch), on host cores."""
@@ -551,7 +557,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config,
+        "config": {**workload_config(args.config, w, algorithmic_bytes(cfg, w.context_lens)),
                    "step": "oracle decode of one sequence of the batch, cycling"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
