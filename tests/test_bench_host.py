@@ -1,6 +1,6 @@
 """Host-side logic of bench.py, on the CPU: the ncu traffic record keyed by
-the kernel source, the clock-sample parser, the roofline denominators and
-the default timing arguments."""
+the kernel source, the clock-sample parser, the roofline denominators, the
+default timing arguments and the reference arm (the CPU oracle) end to end."""
 import hashlib
 import json
 import os
@@ -106,3 +106,36 @@ def test_default_timing_arguments():
 def test_unknown_choices_are_rejected(argv):
     with pytest.raises(SystemExit):
         bench.parse_args(argv)
+
+
+def test_reference_arm_line_on_the_tiny_workload(capsys, monkeypatch):
+    """The reference arm (the CPU oracle) runs here and prints one JSON line
+    with the contract's keys; its config names the workload with the same
+    keys as the native arm's line."""
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    bench.run_reference(bench.parse_args(["--impl", "reference", "--config", "tiny",
+                                          "--steps", "4", "--warmup", "3"]))
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 4 and d["warmup"] == 3
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["metric"] == bench.METRIC
+    c = d["config"]
+    assert c["name"] == "tiny" and c["batch"] == 4 and c["total_context_tokens"] == 310
+    for key in ("workload", "num_q_heads", "num_kv_heads", "head_dim", "block_size",
+                "algorithmic_bytes_per_batch"):
+        assert key in c
+
+
+def test_reference_arm_other_ranks_do_no_work(capsys, monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    bench.run_reference(bench.parse_args(["--impl", "reference", "--config", "tiny",
+                                          "--steps", "2", "--warmup", "3"]))
+    assert capsys.readouterr().out == ""
