@@ -7,6 +7,8 @@ segment's ranges as ``worker_of(first unit) .. worker_of(last unit)`` minus
 empty ranges. This restates that index arithmetic in Python and checks, for
 random batches, that every unit is decoded back to itself, that the combine
 visits exactly the workers that wrote pieces, and that slots never collide.
+The multi-query split's partition (row tiles over the blocks their queries
+can see) is checked the same way.
 """
 
 import random
@@ -49,3 +51,71 @@ def test_partition_slots_and_combine_ranges():
                 for w in ws:
                     assert seg + w not in slots and seg + w < B * hkv + W
                     slots.add(seg + w)
+
+
+# ----------------------------------------------------- multi-query kernel ---
+# The multi-query split orders units (sequence b, kv head, row tile t, block j)
+# over the blocks each 16 NW-row tile can see; row r of a tile is query r // g
+# of the sequence, which sits at position L - n + r // g. A piece of a tile
+# that crosses ranges leaves its rows at slot (b * hkv + kvh) * tmax + t + w.
+
+def tile_blocks(n, L, t, RT, G):
+    q_last = min(n - 1, ((t + 1) * RT - 1) // G)
+    return (L - n + q_last) // 16 + 1
+
+
+def units_per_head(n, L, RT, G):
+    if n == 0:
+        return 0
+    return sum(tile_blocks(n, L, t, RT, G) for t in range(-(-n * G // RT)))
+
+
+def test_multiquery_partition_slots_tiles_and_combine_ranges():
+    rng = random.Random(1)
+    for _ in range(1500):
+        B, hkv = rng.randint(1, 6), rng.randint(1, 3)
+        G, RT = rng.choice([1, 2, 4]), rng.choice([16, 32, 64])
+        max_q = rng.randint(1, 20)
+        ns = [rng.choice([0, 1, rng.randint(0, max_q)]) for _ in range(B)]
+        Ls = [n + rng.randint(0, 90) for n in ns]
+        tmax = -(-max_q * G // RT)
+        prefix = [0]
+        for n, L in zip(ns, Ls):
+            prefix.append(prefix[-1] + hkv * units_per_head(n, L, RT, G))
+        U = prefix[-1]
+        W0 = rng.randint(1, 60)
+        W = max(1, min(W0, U // 4))
+        # brute force: the blocks a tile's rows can see are those up to its
+        # last row's position
+        for n, L in zip(ns, Ls):
+            for t in range(-(-n * G // RT) if n else 0):
+                rows = range(t * RT, min((t + 1) * RT, n * G))
+                last_pos = max(L - n + r // G for r in rows)
+                assert tile_blocks(n, L, t, RT, G) == last_pos // 16 + 1
+        # every unit, in order, and the pieces the split kernel writes
+        order = [(b, k, t, j) for b in range(B) for k in range(hkv)
+                 for t in range(-(-ns[b] * G // RT) if ns[b] else 0)
+                 for j in range(tile_blocks(ns[b], Ls[b], t, RT, G))]
+        assert len(order) == U
+        pieces = {}
+        for w in range(W):
+            for u in range(w * U // W, (w + 1) * U // W):
+                b, k, t, j = order[u]
+                pieces.setdefault((b, k, t), {}).setdefault(w, []).append(j)
+        slots = set()
+        for (b, k, t), by_worker in pieces.items():
+            nb = tile_blocks(ns[b], Ls[b], t, RT, G)
+            per_head = units_per_head(ns[b], Ls[b], RT, G)
+            cum = sum(tile_blocks(ns[b], Ls[b], tt, RT, G) for tt in range(t))
+            uf = prefix[b] + k * per_head + cum
+            ul = uf + nb - 1
+            assert order[uf] == (b, k, t, 0) and order[ul] == (b, k, t, nb - 1)
+            wf, wl = ((uf + 1) * W - 1) // U, ((ul + 1) * W - 1) // U
+            assert set(by_worker) == set(range(wf, wl + 1))
+            if wf == wl:   # finished inside one worker: written directly
+                assert by_worker[wf] == list(range(nb))
+                continue
+            for w in by_worker:
+                s = (b * hkv + k) * tmax + t + w
+                assert s not in slots and s < B * hkv * tmax + W
+                slots.add(s)
