@@ -664,9 +664,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
             __syncwarp();
             // P^T as the B operand: column gq = head gq, tokens 2tq, 2tq + 1 | + 8.
             // P = hi + lo in two parts of the operand type (hi = rn(P), lo =
-            // rn(P - hi), the difference exact in fp32), so the weights keep
-            // ~2^-18 relative precision: with one 16-bit P a two-token context
-            // would be off by up to 2^-9 |v|.
+            // rn(P - hi), the difference exact in fp32), so a weight in [0, 1]
+            // is off by at most 2^-18 (bf16): with one 16-bit P a two-token
+            // context would be off by up to 2^-9 |v|.
             uint32_t ph[2] = {0u, 0u}, pl[2] = {0u, 0u};
             if (gq < G) {
 #pragma unroll
