@@ -1,15 +1,18 @@
 """Benchmark: one decode step of paged-KV attention on GB300.
 
-A step is the whole hot path for one batch: append the step's new K/V token
-per sequence into the paged cache (pkv_append), then paged decode attention
-(pkv_decode_split + pkv_decode_combine). Default workload: the GQA
-Llama-3-8B-shape batch (B=256, 32 q / 8 kv heads, D=128, bf16, L~U[128,4096]).
+A step is the whole hot path for one batch: write the step's new K/V token
+per sequence into the paged cache, then paged decode attention with its
+split-K combine. For fp16/bf16 caches the write is folded into the split
+kernel (pkv_decode_step + pkv_decode_combine, 2 launches; --unfused runs
+pkv_append + pkv_decode_split + pkv_decode_combine); INT8 caches run
+pkv_append + split + combine. Default workload: the GQA Llama-3-8B-shape
+batch (B=256, 32 q / 8 kv heads, D=128, bf16, L~U[128,4096]).
 
     python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
 
 Prints one JSON line. `value` is the decode-attention HBM throughput of the
 whole step: algorithmic bytes (KV + q + block tables, per the workload) over
-the step time, summed over ranks. The KV cache (2.2 GB) is far larger than L2,
+the step time, summed over ranks. The KV cache (2.3 GB) is far larger than L2,
 so no flush is needed between steps. `--impl reference` times the CPU oracle
 (float64 NumPy) on the host cores over a bounded sample of the same workload.
 """
