@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -42,6 +43,18 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+# Kernel-timing pass: CUDA events around every kernel of each step. Events
+# between two launches stop the second from overlapping the first (programmatic
+# dependent launch), so this pass is separate from the timed region; its first
+# KERNEL_PASS_SKIP steps are dropped and the median is reported.
+KERNEL_PASS_MIN_STEPS = 200
+KERNEL_PASS_MIN_MS = 1000.0
+KERNEL_PASS_MAX_STEPS = 20000
+KERNEL_PASS_SKIP = 5
+# Parity bound of the bench's parity leg: bf16 / fp16 KV elementwise
+# |g - o| <= 2e-3 + 1e-2 |o|; INT8 KV |g - o| <= 2e-2 against the oracle on
+# the dequantised cache.
+TOL_ABS, TOL_REL, TOL_I8 = 2e-3, 1e-2, 2e-2
 
 
 def parse_args(argv=None):
@@ -67,10 +80,10 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--event-every", type=int, default=8,
-                    help="record CUDA events around the kernels of every n-th timed step "
-                         "(0: time the kernels in a separate pass); events between kernels "
-                         "stop a launch from overlapping its predecessor, so not every step")
+    ap.add_argument("--kernel-steps", type=int, default=0,
+                    help="steps of the kernel-timing pass that follows the timed region "
+                         "(0: at least %d steps and about %.0f s of work)"
+                         % (KERNEL_PASS_MIN_STEPS, KERNEL_PASS_MIN_MS / 1e3))
     return ap.parse_args(argv)
 
 
@@ -96,19 +109,32 @@ def load_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def kernel_source_hash(source: str = "decode.cu") -> str:
+    """sha256 (first 16 hex digits) of the device code a kernel is built from:
+    ``source`` up to its host-code marker line (``// ---- ... host ---``),
+    followed by common.cuh. Host-side edits below the marker leave it alone."""
+    import hashlib
+    csrc = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc")
+    with open(os.path.join(csrc, source), "rb") as f:
+        text = f.read()
+    m = re.search(rb"^// -+ host -+$", text, re.M)
+    if m:
+        text = text[:m.start()]
+    with open(os.path.join(csrc, "common.cuh"), "rb") as f:
+        text += f.read()
+    return hashlib.sha256(text).hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, config: str, source: str = "decode.cu"):
     """DRAM bytes per launch from the committed ncu summary, if still current.
 
     profiles/<kernel>_<config>.md carries a line
     ``traffic_bytes_per_launch: N source_sha256: H``; it counts only while H
-    matches the current kernel source (``source`` followed by common.cuh).
+    matches :func:`kernel_source_hash` of ``source``.
     """
-    import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
-    csrc = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc")
     try:
-        body = b"".join(open(os.path.join(csrc, f), "rb").read() for f in (source, "common.cuh"))
-        h = hashlib.sha256(body).hexdigest()[:16]
+        h = kernel_source_hash(source)
         for line in open(path):
             if line.startswith("traffic_bytes_per_launch:"):
                 parts = line.split()
@@ -146,7 +172,12 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def stop(self, t0: float, t1: float):
+    def stop(self, t0: float, t1: float, timed=None):
+        """Median SM clock and the throttle reasons seen in the window [t0, t1]
+        (host wall time). ``timed``: the timed region's (start, end) inside
+        that window; its sample count is reported beside the window's (a short
+        timed region can fall between two 100 ms samples, so the window also
+        covers the warm-up and the kernel-timing pass around it)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -155,7 +186,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, reasons, n = [], None, set(), 0
+        sm, smax, reasons, n, n_timed = [], None, set(), 0, 0
         for ts, line in self.lines:
             if not (t0 <= ts <= t1):
                 continue
@@ -168,12 +199,19 @@ class ClockSampler:
             except ValueError:
                 continue
             n += 1
+            if timed is not None and timed[0] <= ts <= timed[1]:
+                n_timed += 1
             for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                                   "sw_power_cap"), f[3:7]):
                 if val.lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": n}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+               "reasons": sorted(reasons), "samples": n}
+        if timed is not None:
+            out["samples_in_timed_region"] = n_timed
+            out["window_s"] = round(t1 - t0, 3)
+            out["window"] = "warm-up, timed steps and kernel-timing pass"
+        return out
 
 
 def _dist():
@@ -221,19 +259,37 @@ def oracle_sample(w, budget_s: float, first: int = 0):
         k = np.zeros(shape, dt); v = np.zeros(shape, dt); ks = vs = None
         oracle.append_copy(k, v, w.k_fill, w.v_fill, w.fill_slots)
         oracle.append_copy(k, v, w.k_step, w.v_step, w.step_slots)
-    seqs, t_total = [], 0.0
+    seqs, outs, t_total = [], {}, 0.0
     b = first
     while len(seqs) < cfg.batch and (t_total < budget_s or not seqs):
         t0 = time.perf_counter()
-        oracle.paged_decode_attention(w.q, k, v, w.block_tables, w.context_lens,
-                                      cfg.softmax_scale, ks, vs, seqs=[b])
+        o = oracle.paged_decode_attention(w.q, k, v, w.block_tables, w.context_lens,
+                                          cfg.softmax_scale, ks, vs, seqs=[b])
         t_total += time.perf_counter() - t0
+        outs[b] = o[b]
         seqs.append(b)
         b = (b + 1) % cfg.batch
     lens = w.context_lens[seqs]
     from paged_kv_decode_05_gb300.workloads import variant
     byts = algorithmic_bytes(variant(cfg, batch=len(seqs)), lens)
-    return t_total, byts, seqs, _threads()
+    return t_total, byts, seqs, _threads(), outs
+
+
+def parity_report(got: dict, want: dict, int8: bool) -> dict:
+    """Element-wise comparison of the GPU output rows with the oracle's on the
+    sampled sequences: max |g - o|, max |g - o| / |o| over |o| >= 0.2, and
+    whether every element meets the workload's bound."""
+    g = np.concatenate([np.asarray(got[b], np.float64).ravel() for b in sorted(want)])
+    o = np.concatenate([np.asarray(want[b], np.float64).ravel() for b in sorted(want)])
+    err = np.abs(g - o)
+    big = np.abs(o) >= 0.2
+    ok = bool(np.all(err <= TOL_I8)) if int8 else bool(np.all(err <= TOL_ABS + TOL_REL * np.abs(o)))
+    return {"sequences": len(want), "elements": int(g.size),
+            "max_abs": float(err.max()) if g.size else 0.0,
+            "max_rel_where_abs_o_ge_0.2": float((err[big] / np.abs(o[big])).max()) if big.any()
+            else 0.0,
+            "bound": "|g-o| <= 2e-2" if int8 else "|g-o| <= 2e-3 + 1e-2|o|", "pass": ok,
+            "against": "float64 oracle" + (" on the dequantised cache" if int8 else "")}
 
 
 def _threads() -> int:
@@ -284,6 +340,32 @@ def _gpu_state(w, device):
     st["out"] = torch.empty_like(st["q"])
     torch.cuda.synchronize(device)
     return st
+
+
+def out_to_f64(t) -> np.ndarray:
+    """A CUDA output tensor (fp16 / bf16) as float64 on the host, exactly."""
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def kernel_pass(step, n: int, device, names=("append", "split", "combine")) -> dict:
+    """Run ``n`` steps, each ``step(ev)`` recording len(names) + 1 CUDA events
+    on the launching stream around its kernels, and return the median, mean,
+    min and max of each kernel's time in ms over the steps after the first
+    KERNEL_PASS_SKIP."""
+    import torch
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1))
+           for _ in range(n)]
+    torch.cuda.synchronize(device)
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize(device)
+    skip = min(KERNEL_PASS_SKIP, max(0, n - 1))
+    res = {"steps": n - skip, "skipped": skip}
+    for i, name in enumerate(names):
+        t = [e[i].elapsed_time(e[i + 1]) for e in evs[skip:]]
+        res[name] = {"median": statistics.median(t), "mean": sum(t) / len(t),
+                     "min": min(t), "max": max(t)}
+    return res
 
 
 def _step(st, cfg, ws, parts, ev=None, fused=None):
@@ -348,6 +430,13 @@ def run_native(args):
     launches_per_step = 2 if st["fused"] else (6 if cfg.kv_dtype == "i8" else 3)
     K, W = args.steps, args.warmup
 
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(str(getattr(props, "uuid", local)).strip())
+    if str(sampler.gpu_id) and not str(sampler.gpu_id).startswith("GPU-"):
+        sampler.gpu_id = "GPU-" + sampler.gpu_id
+    sampler.start()
+    time.sleep(0.3)                 # nvidia-smi is up before the GPU work starts
+    wall_w = time.time()
     for _ in range(W):
         _step(st, cfg, ws, parts)
     torch.cuda.synchronize(device)
@@ -360,49 +449,43 @@ def run_native(args):
             graph.replay()
         torch.cuda.synchronize(device)
 
-    # ---- device-timed region: K steps, inputs resident in HBM
-    every = args.event_every
-    sampled = list(range(0, K, every)) if every > 0 else list(range(K))
-    step_ev = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for i in sampled}
+    # ---- device-timed region: K steps, inputs resident in HBM, no events
+    # between the launches
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    props = torch.cuda.get_device_properties(device)
-    sampler = ClockSampler(str(getattr(props, "uuid", local)).strip())
-    if str(sampler.gpu_id) and not str(sampler.gpu_id).startswith("GPU-"):
-        sampler.gpu_id = "GPU-" + sampler.gpu_id
-    sampler.start()
-    time.sleep(0.5)
     barrier(world, device)
     torch.cuda.synchronize(device)
     wall0 = time.time()
     t_start.record()
-    for i in range(K):
+    for _ in range(K):
         if graph is not None:
             graph.replay()
         else:
-            _step(st, cfg, ws, parts, step_ev.get(i) if every > 0 else None)
+            _step(st, cfg, ws, parts)
     t_end.record()
     torch.cuda.synchronize(device)
     wall1 = time.time()
     barrier(world, device)
-    time.sleep(0.2)
-    clocks = sampler.stop(wall0, wall1)
     ms_total = reduce_max(t_start.elapsed_time(t_end), world, device)
-    if every <= 0 or graph is not None:  # time the kernels in a separate pass of K steps
-        for i in range(K):
-            _step(st, cfg, ws, parts, step_ev.get(i))
-        torch.cuda.synchronize(device)
-    evs = list(step_ev.values())
-    avg = lambda i, j: sum(e[i].elapsed_time(e[j]) for e in evs) / len(evs)  # noqa: E731
-    append_avg_ms, split_avg_ms, combine_avg_ms = avg(0, 1), avg(1, 2), avg(2, 3)
+    out_timed = st["out"].clone()
     status = int(st["status"].item())
+
+    # ---- kernel-timing pass: events around every kernel of each step
+    n_kp = args.kernel_steps or int(min(KERNEL_PASS_MAX_STEPS,
+                                        max(KERNEL_PASS_MIN_STEPS,
+                                            KERNEL_PASS_MIN_MS * K / max(ms_total, 1e-6))))
+    kp = kernel_pass(lambda ev: _step(st, cfg, ws, parts, ev), n_kp, device)
+    wall2 = time.time()
 
     # ---- end-to-end through the C ABI with host buffers (H2D inputs, D2H output)
     e2e = _e2e(st, w, cfg, ws, parts, device, min(K, args.e2e_steps), world)
+    time.sleep(0.2)
+    clocks = sampler.stop(wall_w, wall2, timed=(wall0, wall1))
 
     step_s = ms_total / 1e3 / K
     value = alg * world / step_s / 1e9
     peak, peak_src = load_peaks()
-    achieved = alg / (split_avg_ms / 1e3) / 1e9
+    split_ms = kp["split"]["median"]
+    achieved = alg / (split_ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_total / K, 6),
@@ -423,23 +506,26 @@ def run_native(args):
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic("decode_split_kernel", args.config),
-                     "split_ms_avg": round(split_avg_ms, 6)},
-        "kernel_ms_avg": {"append": round(append_avg_ms, 6), "split": round(split_avg_ms, 6),
-                          "combine": round(combine_avg_ms, 6),
-                          "timed_launches": len(evs),
-                          "how": f"CUDA events around the kernels of every {every}-th timed step"
-                                 if every > 0 and graph is None
-                                 else "CUDA events, separate eager pass of K steps"},
+                     "algorithmic_bytes_per_launch": alg,
+                     "split_ms": round(split_ms, 6),
+                     "split_share_of_step": round(split_ms / (ms_total / K), 4)},
+        "kernel_ms": {**{k: {kk: round(vv, 6) for kk, vv in v.items()}
+                         for k, v in kp.items() if isinstance(v, dict)},
+                      "steps": kp["steps"], "skipped": kp["skipped"],
+                      "how": "separate pass after the timed region: CUDA events around each "
+                             "kernel of every step (the first steps dropped), median"},
         "launch_mode": "cuda_graph" if graph is not None else "eager",
         "e2e": e2e, "gpu_launches": K * launches_per_step, "clocks": clocks,
         "device_status": status,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        t, byts, seqs, thr = oracle_sample(w, args.cpu_budget_s)
+        t, byts, seqs, thr, want = oracle_sample(w, args.cpu_budget_s)
         line["cpu_baseline"] = {"value": round(byts / t / 1e9, 4), "unit": "GB/s", "cores": thr,
                                 "kind": "oracle",
                                 "sample": f"float64 oracle attention over {len(seqs)} of "
                                           f"{cfg.batch} sequences ({t:.1f} s), same workload"}
+        got = out_to_f64(out_timed)
+        line["parity"] = parity_report({b: got[b] for b in want}, want, cfg.kv_dtype == "i8")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -644,30 +730,32 @@ def run_multiquery(args):
         if ev is not None:
             ev[2].record()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
-    evs = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
-           for i in range(0, args.steps, max(1, args.event_every))}
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(device)
     sampler = ClockSampler(str(getattr(props, "uuid", 0)).strip())
     if str(sampler.gpu_id) and not str(sampler.gpu_id).startswith("GPU-"):
         sampler.gpu_id = "GPU-" + sampler.gpu_id
     sampler.start()
-    time.sleep(0.5)
+    time.sleep(0.3)
+    wall_w = time.time()
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     a.record()
-    for i in range(args.steps):
-        step(evs.get(i))
+    for _ in range(args.steps):
+        step()
     b.record()
     torch.cuda.synchronize(device)
     wall1 = time.time()
-    time.sleep(0.2)
-    clocks = sampler.stop(wall0, wall1)
     ms = a.elapsed_time(b) / args.steps
-    attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs.values()) / len(evs)
+    n_kp = args.kernel_steps or int(min(KERNEL_PASS_MAX_STEPS, max(
+        KERNEL_PASS_MIN_STEPS, KERNEL_PASS_MIN_MS / max(ms, 1e-6))))
+    kp = kernel_pass(step, n_kp, device, names=("append", "attn"))
+    wall2 = time.time()
+    time.sleep(0.2)
+    clocks = sampler.stop(wall_w, wall2, timed=(wall0, wall1))
+    attn_ms = kp["attn"]["median"]
     alg = algorithmic_bytes(cfg, w.context_lens)
     lens = w.context_lens.astype(np.int64)
     # causal FLOPs: query i of a sequence attends to L - nq + i + 1 tokens, 4 D flops each head

@@ -6,6 +6,7 @@ import json
 import os
 import types
 
+import numpy as np
 import pytest
 
 import bench
@@ -34,6 +35,25 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     # so does a change to the shared header
     (csrc / "decode.cu").write_bytes(b"kernel v1")
     (csrc / "common.cuh").write_bytes(b"helpers v2")
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") is None
+
+
+def test_traffic_record_ignores_host_code_below_the_marker(tmp_path, monkeypatch):
+    """Only the device code counts: an edit below the host-code marker (an
+    entry point, an argument check) keeps the ncu record current; an edit
+    above it (a kernel) does not."""
+    device = b"__global__ void k() {}\n"
+    host = b"// ------------------------------------------------ host ---\nint f() { return 1; }\n"
+    csrc, _ = _fake_tree(tmp_path, body=device + host)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = hashlib.sha256(device + b"helpers").hexdigest()[:16]
+    assert bench.kernel_source_hash("decode.cu") == h
+    prof = tmp_path / "profiles" / "decode_split_kernel_gqa8b.md"
+    prof.write_text(f"traffic_bytes_per_launch: 99 source_sha256: {h}\n")
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") == 99
+    (csrc / "decode.cu").write_bytes(device + host + b"int g() { return 2; }\n")
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") == 99
+    (csrc / "decode.cu").write_bytes(b"__global__ void k2() {}\n" + host)
     assert bench.recorded_traffic("decode_split_kernel", "gqa8b") is None
 
 
@@ -77,6 +97,35 @@ def test_clock_sampler_keeps_the_timed_window_and_reasons():
     assert c["samples"] == 3
     assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0
     assert c["reasons"] == ["sw_power_cap"]   # the hw_slowdown sample lies outside the window
+
+
+def test_clock_sampler_counts_the_timed_region_inside_its_window():
+    lines = [(t / 10, "2070, 2070, 900.0, Not Active, Not Active, Not Active, Not Active")
+             for t in range(10, 31)]   # samples at 1.0, 1.1, ... 3.0 s
+    c = _sampler(lines).stop(1.0, 3.0, timed=(2.05, 2.25))
+    assert c["samples"] == 21 and c["samples_in_timed_region"] == 2
+    assert c["window_s"] == 2.0 and "timed" in c["window"]
+
+
+def test_parity_report():
+    want = {0: np.array([[1.0, -0.5], [0.1, 0.0]]), 3: np.array([[2.0, 0.25], [0.0, 0.0]])}
+    got = {b: v + 1e-3 for b, v in want.items()}
+    r = bench.parity_report(got, want, int8=False)
+    assert r["pass"] and r["sequences"] == 2 and r["elements"] == 8
+    assert abs(r["max_abs"] - 1e-3) < 1e-12
+    assert abs(r["max_rel_where_abs_o_ge_0.2"] - 1e-3 / 0.25) < 1e-9
+    got[3] = want[3] + np.array([[0.0, 0.0], [0.0, 3e-3]])   # beyond 2e-3 + 1e-2 * 0
+    assert not bench.parity_report(got, want, int8=False)["pass"]
+    assert bench.parity_report(got, want, int8=True)["pass"]   # INT8 bound 2e-2
+    got[0] = want[0] + 0.03
+    assert not bench.parity_report(got, want, int8=True)["pass"]
+
+
+def test_kernel_source_hash_of_the_shipped_sources():
+    """The committed profile summaries carry hashes of this form."""
+    for src in ("decode.cu", "mq.cu"):
+        h = bench.kernel_source_hash(src)
+        assert len(h) == 16 and int(h, 16) >= 0
 
 
 def test_clock_sampler_without_nvidia_smi():
