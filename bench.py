@@ -266,7 +266,7 @@ def oracle_sample(w, budget_s: float, first: int = 0):
         o = oracle.paged_decode_attention(w.q, k, v, w.block_tables, w.context_lens,
                                           cfg.softmax_scale, ks, vs, seqs=[b])
         t_total += time.perf_counter() - t0
-        outs[b] = o[b]
+        outs[b] = o[0]
         seqs.append(b)
         b = (b + 1) % cfg.batch
     lens = w.context_lens[seqs]
