@@ -72,6 +72,8 @@ typedef enum {
 #define PKV_DEV_BAD_LENGTH 2u  /* context_len < 0 or > max_blocks_per_seq*16   */
 #define PKV_DEV_BAD_SLOT   4u  /* slot >= num_blocks*block_size                */
 #define PKV_DEV_TIMEOUT    8u  /* a bounded wait on an in-kernel copy ran out  */
+#define PKV_DEV_BAD_INDEX 16u  /* pkv_merge_states: a row's range of states
+                                  lies outside [0, num_states]              */
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
 
@@ -147,8 +149,9 @@ pkv_status pkv_append(const void *k_new, const void *v_new, pkv_dtype src_dtype,
 
 /* The default num_parts on `device`: the split kernel's resident worker
  * warps, capped at 2 CTAs (8 warps) per SM for fp16/bf16 caches at head_dim
- * 128, where fewer, longer workers read the cache faster. 0 if the
- * configuration is unsupported. */
+ * 128, where fewer, longer workers read the cache faster; INT8 caches run
+ * CTAs of 6 warps, two per SM at batch 256 (fewer CTAs fit for much larger
+ * batches). 0 if the configuration is unsupported. */
 int32_t pkv_decode_default_parts(int32_t device, int32_t batch, int32_t num_q_heads,
                                  const pkv_cache_desc *cache);
 
@@ -211,6 +214,42 @@ pkv_status pkv_decode_combine(const pkv_cache_desc *cache, int32_t batch,
                               int32_t num_q_heads, pkv_dtype out_dtype, void *out,
                               const void *workspace, size_t workspace_bytes,
                               int32_t num_parts, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Merge of partial attention states (the split-K reduce on its own)
+ *
+ * Attention over a set of tokens may be computed piece by piece: piece i
+ * leaves the state (m_i, l_i, o_i), m_i its largest score, l_i = sum_t
+ * exp(s_t - m_i) and o_i = sum_t exp(s_t - m_i) v_t (unnormalised, natural
+ * exponent). The attention over the union of the pieces is
+ *   out = sum_i exp(m_i - M) o_i / sum_i exp(m_i - M) l_i,   M = max_i m_i,
+ * whatever the partition: the flash-decoding reduce that pkv_decode_combine
+ * applies to the split kernel's own pieces. This call merges states the
+ * caller brings, e.g. the pieces of one sequence computed on several GPUs and
+ * gathered (the decode kernel's work split is described under "Decode
+ * attention"; the pages name no reduce, so its form is the split identity
+ * above).
+ *
+ * part_m, part_l  fp32 [num_states, num_heads]
+ * part_o          fp32 [num_states, num_heads, head_dim], 16-byte aligned
+ * row_ptr         int32 [num_rows + 1], non-decreasing: row r merges states
+ *                 row_ptr[r] .. row_ptr[r+1] - 1 (a range outside
+ *                 [0, num_states] is flagged PKV_DEV_BAD_INDEX, row zeroed)
+ * out             [num_rows, num_heads, head_dim] in out_dtype (PKV_F16 or
+ *                 PKV_BF16), fp32 arithmetic, rounded to nearest even;
+ *                 8-byte aligned
+ * out_m, out_l    optional fp32 [num_rows, num_heads]: the merged M and
+ *                 sum_i exp(m_i - M) l_i, so that (out_m, out_l, out * out_l)
+ *                 is itself a state of the union
+ * A state with m = -inf (or NaN) or l <= 0 contributes nothing; a row with no
+ * other state gets zeros (out_m = -inf, out_l = 0). head_dim: a multiple of
+ * 4, at most 512. All arrays are device memory.
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_merge_states(const float *part_m, const float *part_l, const float *part_o,
+                            int64_t num_states, const int32_t *row_ptr, int32_t num_rows,
+                            int32_t num_heads, int32_t head_dim, pkv_dtype out_dtype,
+                            void *out, float *out_m, float *out_l, uint32_t *dev_status,
+                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Multi-query attention: speculative verification and prefill chunks

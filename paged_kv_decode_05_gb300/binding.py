@@ -17,7 +17,7 @@ from .build import LIB, up_to_date
 PKV_F16, PKV_BF16, PKV_I8 = 0, 1, 2
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
           3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}
-DEV_BAD_BLOCK, DEV_BAD_LENGTH, DEV_BAD_SLOT, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_BLOCK, DEV_BAD_LENGTH, DEV_BAD_SLOT, DEV_TIMEOUT, DEV_BAD_INDEX = 1, 2, 4, 8, 16
 BLOCK_SIZE = 16
 
 
@@ -61,6 +61,17 @@ _SIGS = {
                                            _P, _P]),
     "pkv_decode_attn_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32,
                                                _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P]),
+    "pkv_merge_states": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P, _I32, _I32, _I32,
+                                        ctypes.c_int, _P, _P, _P, _P, _P]),
+    # test hooks (include/pkv_testing.h)
+    "pkv_testing_decode_attn_stall": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P,
+                                                     _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
+                                                     _SZ, _I32, ctypes.c_uint64, _I32,
+                                                     _P, _P]),
+    "pkv_testing_multiquery_attn_stall": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _DESC,
+                                                         _P, _I32, _P, _I32, _I32, ctypes.c_float,
+                                                         _P, _P, _SZ, _I32, ctypes.c_uint64,
+                                                         _I32, _P, _P]),
 }
 
 
@@ -250,3 +261,45 @@ def pkv_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, sof
         B, Hq, float(softmax_scale), _ptr(out), int(num_parts), _ptr(dev_status),
         _stream(stream))
     _check("pkv_decode_attn_noalloc", code)
+
+
+def pkv_merge_states(part_m, part_l, part_o, row_ptr, out, out_m=None, out_l=None,
+                     dev_status=None, stream=None):
+    """Merge partial states ``(m, l, o)`` (``[S, H]``, ``[S, H]``, ``[S, H, D]`` fp32):
+    row ``r`` of ``out [R, H, D]`` merges states ``row_ptr[r] .. row_ptr[r+1]-1``."""
+    S, H, D = part_o.shape
+    R = int(row_ptr.numel()) - 1
+    code = lib().pkv_merge_states(_ptr(part_m), _ptr(part_l), _ptr(part_o), int(S),
+                                  _ptr(row_ptr), R, int(H), int(D), _dtype_code(out), _ptr(out),
+                                  _ptr(out_m), _ptr(out_l), _ptr(dev_status), _stream(stream))
+    _check("pkv_merge_states", code)
+
+
+def pkv_testing_decode_attn_stall(q, k_cache, v_cache, block_tables, context_lens, softmax_scale,
+                                  out, workspace, wait_limit_ns, stall_worker, k_scales=None,
+                                  v_scales=None, num_parts=0, dev_status=None, stream=None):
+    """Test hook: :func:`pkv_decode_attn` whose worker ``stall_worker`` never completes
+    the wait for its first unit (bounded by ``wait_limit_ns``); see ``include/pkv_testing.h``."""
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    code = lib().pkv_testing_decode_attn_stall(
+        _ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        B, Hq, float(softmax_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(num_parts), int(wait_limit_ns),
+        int(stall_worker), _ptr(dev_status), _stream(stream))
+    _check("pkv_testing_decode_attn_stall", code)
+
+
+def pkv_testing_multiquery_attn_stall(q, cu_q, max_q_len, k_cache, v_cache, block_tables,
+                                      context_lens, softmax_scale, out, workspace, wait_limit_ns,
+                                      stall_cta, num_parts=0, dev_status=None, stream=None):
+    """Test hook: :func:`pkv_multiquery_attn` whose CTA ``stall_cta`` stalls."""
+    desc = cache_desc(k_cache)
+    code = lib().pkv_testing_multiquery_attn_stall(
+        _ptr(q), _dtype_code(q), _ptr(cu_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        int(cu_q.numel() - 1), int(q.shape[1]), float(softmax_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(num_parts), int(wait_limit_ns),
+        int(stall_cta), _ptr(dev_status), _stream(stream))
+    _check("pkv_testing_multiquery_attn_stall", code)

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["append.cu", "decode.cu", "blocks.cu", "mq.cu"]
+SOURCES = ["append.cu", "decode.cu", "blocks.cu", "mq.cu", "merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 
@@ -36,7 +36,7 @@ def nvcc() -> str:
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    files.append(os.path.join(INCLUDE, "pkv.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return files
 
 

@@ -37,8 +37,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarpsPerCta = 4;
-constexpr int kThreads = kWarpsPerCta * 32;
+constexpr int kMaxWarpsPerCta = 8;   // scan scratch slots at the start of shared memory
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms when draining
 constexpr int kMaxBatch = 8192;
@@ -55,9 +54,14 @@ template <typename KV, int D, int G>
 struct Cfg {
     static constexpr int esize = Elem<KV>::bytes;
     static constexpr int kI8 = (esize == 1);
+    // Blocks per work unit: 2 for INT8 caches (a unit of 32 tokens halves the
+    // per-token share of the softmax bookkeeping, the waits and the copy
+    // issue, which bound the INT8 kernel), 1 for 16-bit caches.
+    static constexpr int UB = kI8 ? 2 : 1;
+    static constexpr int UT = UB * kBlockSize;                    // tokens per unit
     static constexpr int TILE = kBlockSize * D * esize;          // bytes of one K (or V) tile
     static constexpr int ROW = D * esize;                         // bytes of one token row
-    static constexpr int STAGE = 2 * TILE;
+    static constexpr int STAGE = 2 * UB * TILE;                   // K tiles [UB], V tiles [UB]
     // Stages per warp: as many as fit ~19 KB per warp with their q slots, so
     // that 3 CTAs of 4 warps share an SM (at least 2 stages).
     static constexpr int QBYTES = G * D * 2;   // q rows of one (sequence, kv head)
@@ -65,19 +69,32 @@ struct Cfg {
     // Per-warp shared-memory region.
     static constexpr int OFF_BAR = NS * STAGE;                       // 8-byte mbarriers
     static constexpr int OFF_META = align_up(OFF_BAR + NS * 8, 16);   // int4 per stage
-    static constexpr int OFF_SCL = OFF_META + NS * 16;                // float2 per stage
-    static constexpr int OFF_P = align_up(OFF_SCL + NS * 8, 16);      // float4 reads
+    static constexpr int OFF_SCL = OFF_META + NS * 16;                // float2 per stage, block
+    static constexpr int OFF_P = align_up(OFF_SCL + NS * UB * 8, 16); // float4 reads
+    // P[head][token] rows in shared memory: UT floats each
+    static constexpr int PS = UT;
     // q rows of a piece's (sequence, kv head), copied with its first unit
-    static constexpr int OFF_Q = align_up(OFF_P + kBlockSize * G * 4, 128);
+    static constexpr int OFF_Q = align_up(OFF_P + PS * G * 4, 128);
     static constexpr int WARP_BYTES = align_up(OFF_Q + NS * QBYTES, 128);
+    // Worker warps per CTA: 4 (three CTAs share an SM); INT8 units take more
+    // shared memory than three 4-warp CTAs can have, so INT8 runs CTAs of 6
+    // warps, two per SM (228 KB of shared memory, 1 KB reserved per CTA),
+    // whenever a batch of 256 still fits, which keeps 12 warps per SM.
+    static constexpr int kSmemPerSm = 233472, kReservedPerCta = 1024;
+    static constexpr int WARPS =
+        (kI8 && 2 * (6 * WARP_BYTES + 1152 + kReservedPerCta) <= kSmemPerSm) ? 6 : 4;
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int MIN_CTAS = WARPS == 6 ? 2 : 3;   // launch bounds: registers per thread
     static_assert(NS >= 2 && NS <= 32, "stage count (one parity bit per stage)");
     static_assert(STAGE % 128 == 0 && OFF_Q % 128 == 0 && QBYTES % 16 == 0, "copy alignment");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size (heads fill <= 8 MMA columns)");
 };
 
-// Dynamic shared memory starts with 4 ints of scan scratch, then the block
-// prefix [batch + 1]; the per-warp regions follow, 128-byte aligned.
-__host__ __device__ inline int prefix_bytes(int batch) { return align_up(16 + 4 * (batch + 1), 128); }
+// Dynamic shared memory starts with kMaxWarpsPerCta ints of scan scratch, then
+// the block prefix [batch + 1]; the per-warp regions follow, 128-byte aligned.
+__host__ __device__ inline int prefix_bytes(int batch) {
+    return align_up(4 * kMaxWarpsPerCta + 4 * (batch + 1), 128);
+}
 
 // Workers that get units: at most one per kMinUnits units, so every range is
 // non-empty and short batches are not cut into single-block pieces. The split
@@ -105,6 +122,9 @@ struct DecodeParams {
     const void* v_new;    // (nullptr: attention only)
     int batch, hq, hkv, mb, num_blocks, workers;
     float qscale;         // softmax_scale * log2(e)
+    uint64_t wait_ns;     // limit of each bounded wait on a stage (kWaitLimitNs)
+    int stall_worker;     // test hook: this worker's first stage expects 16 bytes no
+                          // copy delivers, so its wait runs out (-1: none)
 };
 
 __device__ __forceinline__ int clamp_len(int L, int mb, uint32_t* status, bool flag) {
@@ -115,15 +135,17 @@ __device__ __forceinline__ int clamp_len(int L, int mb, uint32_t* status, bool f
     return L;
 }
 
-// prefix[b] = sum_{b' < b} ceil(L_b' / 16) for b in [0, batch]; all threads.
+// prefix[b] = sum_{b' < b} ceil(L_b' / UT) for b in [0, batch], UT = tokens
+// per unit (16 UB); all threads.
+template <int UT, int NT>
 __device__ void build_prefix(const DecodeParams& p, int* warp_tot, int* prefix) {
     const int t = threadIdx.x;
-    const int chunk = (p.batch + kThreads - 1) / kThreads;
+    const int chunk = (p.batch + NT - 1) / NT;
     const int lo = min(p.batch, t * chunk), hi = min(p.batch, lo + chunk);
     const bool flag = blockIdx.x == 0;
     int sum = 0;
     for (int i = lo; i < hi; ++i)
-        sum += (clamp_len(p.context_lens[i], p.mb, p.status, flag) + kBlockSize - 1) / kBlockSize;
+        sum += (clamp_len(p.context_lens[i], p.mb, p.status, flag) + UT - 1) / UT;
     // exclusive scan of per-thread sums across the CTA
     const int lane = t & 31, warp = t >> 5;
     int inc = sum;
@@ -139,16 +161,17 @@ __device__ void build_prefix(const DecodeParams& p, int* warp_tot, int* prefix) 
     int run = base + inc - sum;
     for (int i = lo; i < hi; ++i) {
         prefix[i] = run;
-        run += (clamp_len(p.context_lens[i], p.mb, p.status, false) + kBlockSize - 1) / kBlockSize;
+        run += (clamp_len(p.context_lens[i], p.mb, p.status, false) + UT - 1) / UT;
     }
-    if (t == kThreads - 1) prefix[p.batch] = run;
+    if (t == NT - 1) prefix[p.batch] = run;
     __syncthreads();
     if (blockIdx.x == 0)
-        for (int i = t; i <= p.batch; i += kThreads) p.ws_prefix[i] = prefix[i];
+        for (int i = t; i <= p.batch; i += NT) p.ws_prefix[i] = prefix[i];
 }
 
-// Unit u -> (b, kv head, block j): b is the last sequence whose first unit
-// is <= u (it always has blocks, since u < U).
+// Unit u -> (b, kv head, unit j of the segment, i.e. blocks UB j .. UB j + UB - 1):
+// b is the last sequence whose first unit is <= u (it always has blocks,
+// since u < U).
 __device__ __forceinline__ void decode_unit(long long u, const int* prefix, int batch, int hkv,
                                             int& b, int& kvh, int& j) {
     const int x = int(u / hkv);
@@ -188,16 +211,17 @@ __device__ __forceinline__ void store_out(void* out, long long off, const float2
 }
 
 template <typename KV, typename QT, int D, int G>
-__global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(Cfg<KV, D, G>::THREADS, Cfg<KV, D, G>::MIN_CTAS)
+decode_split_kernel(const DecodeParams p) {
     using C = Cfg<KV, D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
-    int* prefix = reinterpret_cast<int*>(smem) + 4;
+    int* prefix = reinterpret_cast<int*>(smem) + kMaxWarpsPerCta;
     griddep_wait();                 // inputs may come from the previous grid
     griddep_launch_dependents();    // the combine may start launching
-    build_prefix(p, reinterpret_cast<int*>(smem), prefix);
+    build_prefix<C::UT, C::THREADS>(p, reinterpret_cast<int*>(smem), prefix);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long w = (long long)blockIdx.x * kWarpsPerCta + warp;
+    const long long w = (long long)blockIdx.x * C::WARPS + warp;
     const long long U = (long long)prefix[p.batch] * p.hkv;
     const long long W = eff_workers(U, p.workers);
     if (w >= W || U == 0) return;
@@ -216,35 +240,77 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     __syncwarp();
 
     // ---- producer: block-table entries for 32 units at a time, one per lane
-    auto fetch = [&](long long base, int& b, int& kvh, int& j, int& blk, int& len) {
+    // (blk1: the unit's second block for two-block units, while the sequence
+    // reaches it)
+    auto fetch = [&](long long base, int& b, int& kvh, int& j, int& blk, int& blk1, int& len) {
         const long long u = base + lane;
+        blk1 = -1;
         if (u < u1) {
             decode_unit(u, prefix, p.batch, p.hkv, b, kvh, j);
-            blk = __ldg(p.block_tables + (long long)b * p.mb + j);
+            const int32_t* row = p.block_tables + (long long)b * p.mb + C::UB * j;
+            blk = __ldg(row);
             len = clamp_len(__ldg(p.context_lens + b), p.mb, p.status, false);
+            if constexpr (C::UB == 2)
+                if ((2 * j + 1) * kBlockSize < len) blk1 = __ldg(row + 1);
         } else {
             b = 0; kvh = 0; j = 0; blk = -1; len = 0;
         }
     };
     long long cbase = u0;
-    int cb, ckvh, cj, cblk, clen, xb, xkvh, xj, xblk, xlen;
-    fetch(cbase, cb, ckvh, cj, cblk, clen);
-    fetch(cbase + 32, xb, xkvh, xj, xblk, xlen);
+    int cb, ckvh, cj, cblk, cblk1, clen, xb, xkvh, xj, xblk, xblk1, xlen;
+    fetch(cbase, cb, ckvh, cj, cblk, cblk1, clen);
+    fetch(cbase + 32, xb, xkvh, xj, xblk, xblk1, xlen);
 
-    auto issue = [&](long long u, int s) {
+    auto issue = [&](long long u, int s, uint32_t extra_tx) {
         int idx = int(u - cbase);
         if (idx >= 32) {
             cbase += 32;
-            cb = xb; ckvh = xkvh; cj = xj; cblk = xblk; clen = xlen;
-            fetch(cbase + 32, xb, xkvh, xj, xblk, xlen);
+            cb = xb; ckvh = xkvh; cj = xj; cblk = xblk; cblk1 = xblk1; clen = xlen;
+            fetch(cbase + 32, xb, xkvh, xj, xblk, xblk1, xlen);
             idx -= 32;
         }
         const int b = __shfl_sync(kFull, cb, idx);
         const int kvh = __shfl_sync(kFull, ckvh, idx);
         const int j = __shfl_sync(kFull, cj, idx);
         const int blk = __shfl_sync(kFull, cblk, idx);
+        const int blk1 = (C::UB == 2) ? __shfl_sync(kFull, cblk1, idx) : -1;
         const int len = __shfl_sync(kFull, clen, idx);
-        if (lane == 0) {
+        if (C::UB == 2 && lane == 0) {
+            // Two-block unit (INT8): blocks 2j and 2j + 1, the second while the
+            // sequence reaches it. K tiles at stage + i TILE, V tiles at stage +
+            // (2 + i) TILE, block i's scales in scl[2 s + i]; meta flag bits:
+            // 0 = block 0 copied, 1 = first unit of a piece, 3 = block 1 copied.
+            const uint32_t bar = smem_addr(&bars[s]);
+            const bool ok0 = unsigned(blk) < unsigned(p.num_blocks);
+            const bool has1 = (2 * j + 1) * kBlockSize < len;
+            const bool ok1 = has1 && unsigned(blk1) < unsigned(p.num_blocks);
+            const bool first = (u == u0) || (j == 0);
+            meta[s] = make_int4(b, kvh | ((ok0 ? 1 : 0) << 16) | ((first ? 1 : 0) << 17) |
+                                       ((ok1 ? 1 : 0) << 19), j, len);
+            const uint32_t tx = (ok0 ? 2 * C::TILE : 0) + (ok1 ? 2 * C::TILE : 0) +
+                                (first ? C::QBYTES : 0) + extra_tx;
+            if (tx) mbar_arrive_expect_tx(bar, tx);
+            else mbar_arrive(bar);
+            if (first)
+                bulk_g2s(smem_addr(region + C::OFF_Q + s * C::QBYTES),
+                         static_cast<const uint16_t*>(p.q) + ((long long)b * p.hq + kvh * G) * D,
+                         C::QBYTES, bar);
+            unsigned char* st = region + s * C::STAGE;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (!(i ? ok1 : ok0)) continue;
+                const long long tile = (long long)(i ? blk1 : blk) * p.hkv + kvh;
+                bulk_g2s(smem_addr(st + i * C::TILE),
+                         static_cast<const char*>(p.k_cache) + tile * C::TILE, C::TILE, bar);
+                bulk_g2s(smem_addr(st + (2 + i) * C::TILE),
+                         static_cast<const char*>(p.v_cache) + tile * C::TILE, C::TILE, bar);
+                cp_async_4(smem_addr(&scl[2 * s + i].x), p.k_scales + tile);
+                cp_async_4(smem_addr(&scl[2 * s + i].y), p.v_scales + tile);
+            }
+            if (ok0 || ok1) cp_async_arrive_noinc(bar);
+            else mbar_arrive(bar);
+            if (!ok0 || (has1 && !ok1)) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+        } else if (C::UB == 1 && lane == 0) {
             const uint32_t bar = smem_addr(&bars[s]);
             const bool ok = unsigned(blk) < unsigned(p.num_blocks);
             const bool first = (u == u0) || (j == 0);   // first unit of a piece
@@ -260,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                                        ((fuse ? 1 : 0) << 18), j, len);
             if (fuse) scl[s].x = __int_as_float(blk);   // scales are unused for 16-bit caches
             const uint32_t tx = (ok ? 2 * (fuse ? (r + 1) * C::ROW : C::TILE) : 0) +
-                                (first ? C::QBYTES : 0);
+                                (first ? C::QBYTES : 0) + extra_tx;
             if (tx) mbar_arrive_expect_tx(bar, tx);
             else mbar_arrive(bar);
             if (first)
@@ -389,25 +455,27 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                 vx16[i][c] = *reinterpret_cast<const uint4*>(row + 16 * (c ^ vswap));
         }
     };
-    uint32_t vw8[4][C::kI8 ? DL / 4 : 1];
-    auto read_v8 = [&](const unsigned char* vt) {
+    uint32_t vw8[C::UB][4][C::kI8 ? DL / 4 : 1];   // INT8: per block of the unit
+    auto read_v8 = [&](const unsigned char* vt, int blk_i) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int t = 2 * tq + (i & 1) + 8 * (i >> 1);
             const unsigned char* row = vt + t * C::ROW + gq * DL;
             if constexpr (DL == 16) {
                 const uint4 x = *reinterpret_cast<const uint4*>(row);
-                vw8[i][0] = x.x; vw8[i][1] = x.y; vw8[i][2] = x.z; vw8[i][3] = x.w;
+                vw8[blk_i][i][0] = x.x; vw8[blk_i][i][1] = x.y;
+                vw8[blk_i][i][2] = x.z; vw8[blk_i][i][3] = x.w;
             } else if constexpr (DL == 8) {
                 const uint2 x = *reinterpret_cast<const uint2*>(row);
-                vw8[i][0] = x.x; vw8[i][1] = x.y;
+                vw8[blk_i][i][0] = x.x; vw8[blk_i][i][1] = x.y;
             }
         }
     };
-    auto load_v = [&](const unsigned char* vt, int nv) {
+    auto load_v = [&](const unsigned char* vt, int nv, int blk_i) {
         if constexpr (!C::kI8) {
             // 16-bit: DL dims of each of the lane's four rows (read by read_v16)
             (void)vt;
+            (void)blk_i;
             uint32_t vw[4][DL / 2];
             const int vswap = (DL / 8 == 2) ? (tq & 1) : 0;
 #pragma unroll
@@ -437,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
             // any byte is a finite code and its P is exactly 0.
             (void)vt;
             (void)nv;
-            auto& vw = vw8;
+            auto& vw = vw8[blk_i];
 #pragma unroll
             for (int k = 0; k < DL / 4; ++k) {
 #pragma unroll
@@ -456,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     };
 
     for (int s = 0; s < C::NS; ++s)
-        if (u0 + s < u1) issue(u0 + s, s);
+        if (u0 + s < u1) issue(u0 + s, s, (s == 0 && w == p.stall_worker) ? 16u : 0u);
     long long u_issue = (u0 + C::NS < u1) ? u0 + C::NS : u1;
     uint32_t parity = 0;
     long long u = u0;
@@ -464,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     int s = 0;                       // stage of unit u
     for (; u < u1; ++u, s = (s + 1 == C::NS) ? 0 : s + 1) {
         const uint32_t bar = smem_addr(&bars[s]);
-        const bool got = mbar_wait_bounded(bar, (parity >> s) & 1u, kWaitLimitNs);
+        const bool got = mbar_wait_bounded(bar, (parity >> s) & 1u, p.wait_ns);
         if (!__all_sync(kFull, got)) {
             if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
             aborted = true;
@@ -531,17 +599,29 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
         }
         last_j = mt.z;
 
-        if (flags & 1) {
-            const unsigned char* kt = region + s * C::STAGE;
-            const unsigned char* vt = kt + C::TILE;
-            const int nv = min(kBlockSize, plen - kBlockSize * mt.z);
-            float ksc = 1.f, vsc = 1.f;
-            // scores S[token][head]: two accumulator chains (even / odd k-steps).
-            // Rows are D * esize bytes apart, a multiple of 128, so all rows
-            // share the bank mapping: lanes of odd gq read the two k-step groups
-            // of a 128-byte span in the other order, which spreads each quarter
-            // warp over all 32 banks, and the groups are put back in registers.
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (flags & (C::UB == 2 ? 9 : 1)) {
+            const unsigned char* kt = region + s * C::STAGE;   // K tiles of the unit
+            const unsigned char* vt = kt + C::UB * C::TILE;    // V tiles
+            const int nv = min(C::UT, plen - C::UT * mt.z);     // valid tokens of the unit
+            float ksc[C::UB], vsc[C::UB];
+            bool okb[C::UB];                                    // block i was copied
+#pragma unroll
+            for (int i = 0; i < C::UB; ++i) {
+                ksc[i] = 1.f;
+                vsc[i] = 1.f;
+                okb[i] = (C::UB == 1) || ((flags >> (i ? 3 : 0)) & 1);
+            }
+            // scores S[token][head] of block i: two accumulator chains (even /
+            // odd k-steps). Rows are D * esize bytes apart, a multiple of 128,
+            // so all rows share the bank mapping: lanes of odd gq read the two
+            // k-step groups of a 128-byte span in the other order, which
+            // spreads each quarter warp over all 32 banks, and the groups are
+            // put back in registers.
+            float acc[C::UB][2][4];
+#pragma unroll
+            for (int i = 0; i < C::UB; ++i)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) acc[i][c][0] = acc[i][c][1] = acc[i][c][2] = acc[i][c][3] = 0.f;
             const bool kswap = !C::kI8 && (gq & 1) != 0;
             if constexpr (!C::kI8) {
                 if (flags & 4) {   // fused step: the new token's row goes to the cache
@@ -573,19 +653,26 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                         const uint4 x1 = sel4(kswap, y[h ^ 1][1], y[h][1]);
                         const uint32_t a0[4] = {x0.x, x1.x, x0.y, x1.y};
                         const uint32_t a1[4] = {x0.z, x1.z, x0.w, x1.w};
-                        mma16816<KV>(acc[0], a0, qb[2 * c][0], qb[2 * c][1]);
-                        mma16816<KV>(acc[1], a1, qb[2 * c + 1][0], qb[2 * c + 1][1]);
+                        mma16816<KV>(acc[0][0], a0, qb[2 * c][0], qb[2 * c][1]);
+                        mma16816<KV>(acc[0][1], a1, qb[2 * c + 1][0], qb[2 * c + 1][1]);
                     }
                 }
                 read_v16(vt);
             } else {
-                const float2 sc = scl[s];
-                ksc = sc.x;
-                vsc = sc.y;
-                if (vsc * vmul >= 16384.f) {   // warp-uniform; raise vexp, rescale O exactly
+                // the blocks' scales (0 for a block that was not copied: its
+                // tokens are masked and its P is 0)
+                float vmax = 0.f;
+#pragma unroll
+                for (int i = 0; i < C::UB; ++i) {
+                    const float2 sc = scl[C::UB * s + i];
+                    ksc[i] = okb[i] ? sc.x : 0.f;
+                    vsc[i] = okb[i] ? sc.y : 0.f;
+                    vmax = fmaxf(vmax, vsc[i]);
+                }
+                if (vmax * vmul >= 16384.f) {   // warp-uniform; raise vexp, rescale O exactly
                     int ex;
-                    frexpf(vsc, &ex);           // vsc < 2^ex
-                    const int nexp = ex - 14;   // vsc * 2^-nexp < 2^14
+                    frexpf(vmax, &ex);          // vmax < 2^ex
+                    const int nexp = ex - 14;   // vmax * 2^-nexp < 2^14
                     const float r = ldexpf(1.f, vexp - nexp);
 #pragma unroll
                     for (int i = 0; i < MT; ++i) {
@@ -595,63 +682,87 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                     vexp = nexp;
                     vmul = ldexpf(1.f, -nexp);
                 }
-                vsc *= vmul;
+#pragma unroll
+                for (int i = 0; i < C::UB; ++i) vsc[i] *= vmul;
                 // the lane's 16-byte chunk of each half row holds 4 k-steps' columns
                 constexpr int NC = D / 64;
-                uint4 y[NC][2];
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const int cc = (NC == 2) ? (c ^ (kswap ? 1 : 0)) : c;
-                    y[c][0] = *reinterpret_cast<const uint4*>(kt + gq * C::ROW + 64 * cc + 16 * tq);
-                    y[c][1] = *reinterpret_cast<const uint4*>(kt + (gq + 8) * C::ROW + 64 * cc + 16 * tq);
-                }
-                uint32_t w0[D / 16], w1[D / 16];
+                for (int bi = 0; bi < C::UB; ++bi) {
+                    const unsigned char* kb = kt + bi * C::TILE;
+                    uint4 y[NC][2];
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const uint4 x0 = (NC == 2) ? sel4(kswap, y[(c ^ 1) & (NC - 1)][0], y[c][0]) : y[c][0];
-                    const uint4 x1 = (NC == 2) ? sel4(kswap, y[(c ^ 1) & (NC - 1)][1], y[c][1]) : y[c][1];
-                    w0[4 * c] = x0.x; w0[4 * c + 1] = x0.y; w0[4 * c + 2] = x0.z; w0[4 * c + 3] = x0.w;
-                    w1[4 * c] = x1.x; w1[4 * c + 1] = x1.y; w1[4 * c + 2] = x1.z; w1[4 * c + 3] = x1.w;
+                    for (int c = 0; c < NC; ++c) {
+                        y[c][0] = *reinterpret_cast<const uint4*>(kb + gq * C::ROW + 64 * c + 16 * tq);
+                        y[c][1] = *reinterpret_cast<const uint4*>(kb + (gq + 8) * C::ROW + 64 * c + 16 * tq);
+                    }
+                    uint32_t w0[D / 16], w1[D / 16];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        w0[4 * c] = y[c][0].x; w0[4 * c + 1] = y[c][0].y;
+                        w0[4 * c + 2] = y[c][0].z; w0[4 * c + 3] = y[c][0].w;
+                        w1[4 * c] = y[c][1].x; w1[4 * c + 1] = y[c][1].y;
+                        w1[4 * c + 2] = y[c][1].z; w1[4 * c + 3] = y[c][1].w;
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t u0 = w0[kk] ^ 0x80808080u, u1 = w1[kk] ^ 0x80808080u;
+                        mma_16816_f16(acc[bi][kk & 1], i8x2_biased_h2(u0, 0x4140),
+                                      i8x2_biased_h2(u1, 0x4140), i8x2_biased_h2(u0, 0x4342),
+                                      i8x2_biased_h2(u1, 0x4342), qb[kk][0], qb[kk][1]);
+                    }
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t u0 = w0[kk] ^ 0x80808080u, u1 = w1[kk] ^ 0x80808080u;
-                    mma_16816_f16(acc[kk & 1], i8x2_biased_h2(u0, 0x4140), i8x2_biased_h2(u1, 0x4140),
-                                  i8x2_biased_h2(u0, 0x4342), i8x2_biased_h2(u1, 0x4342),
-                                  qb[kk][0], qb[kk][1]);
-                }
-                read_v8(vt);
+                for (int bi = 0; bi < C::UB; ++bi) read_v8(vt + bi * C::TILE, bi);
             }
-            const float sk = p.qscale * ksc;
-            float sv[2][2];   // [token gq / gq + 8][head 2tq + e]
+            float sv[C::UB][2][2];   // [block][token gq / gq + 8][head 2tq + e]
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const bool hv = 2 * tq + e < G;
-                float s0 = acc[0][e] + acc[1][e], s1 = acc[0][2 + e] + acc[1][2 + e];
-                if constexpr (C::kI8) {   // the K bias comes off before the scale
-                    s0 -= kbias[e];
-                    s1 -= kbias[e];
+            for (int bi = 0; bi < C::UB; ++bi) {
+                const float sk = p.qscale * ksc[bi];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const bool hv = 2 * tq + e < G && okb[bi];
+                    float s0 = acc[bi][0][e] + acc[bi][1][e], s1 = acc[bi][0][2 + e] + acc[bi][1][2 + e];
+                    if constexpr (C::kI8) {   // the K bias comes off before the scale
+                        s0 -= kbias[e];
+                        s1 -= kbias[e];
+                    }
+                    sv[bi][0][e] = (hv && kBlockSize * bi + gq < nv) ? s0 * sk : -INFINITY;
+                    sv[bi][1][e] = (hv && kBlockSize * bi + gq + 8 < nv) ? s1 * sk : -INFINITY;
                 }
-                sv[0][e] = (hv && gq < nv) ? s0 * sk : -INFINITY;
-                sv[1][e] = (hv && gq + 8 < nv) ? s1 * sk : -INFINITY;
             }
             float alpha[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                float bme = fmaxf(sv[0][e], sv[1][e]);   // block max over the 16 tokens
+                float bme = fmaxf(sv[0][0][e], sv[0][1][e]);   // max over the unit's tokens
+#pragma unroll
+                for (int bi = 1; bi < C::UB; ++bi) bme = fmaxf(bme, fmaxf(sv[bi][0][e], sv[bi][1][e]));
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) bme = fmaxf(bme, __shfl_xor_sync(kFull, bme, off));
                 const float mn = fmaxf(m[e], bme);
                 alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m[e] - mn);
                 m[e] = mn;
-                const float p0 = (sv[0][e] == -INFINITY) ? 0.f : fast_exp2(sv[0][e] - mn);
-                const float p1 = (sv[1][e] == -INFINITY) ? 0.f : fast_exp2(sv[1][e] - mn);
-                lsum[e] = lsum[e] * alpha[e] + p0 + p1;
-                if constexpr (C::kI8) pv[e] = fmaf(pv[e], alpha[e], (p0 + p1) * vsc);
-                if (2 * tq + e < G) {   // P[head][token], times the block's V scale
-                    pbuf[(2 * tq + e) * kBlockSize + gq] = p0 * vsc;
-                    pbuf[(2 * tq + e) * kBlockSize + gq + 8] = p1 * vsc;
+                float ls = lsum[e] * alpha[e], wsum = 0.f;
+#pragma unroll
+                for (int bi = 0; bi < C::UB; ++bi) {
+                    const float p0 = (sv[bi][0][e] == -INFINITY) ? 0.f : fast_exp2(sv[bi][0][e] - mn);
+                    const float p1 = (sv[bi][1][e] == -INFINITY) ? 0.f : fast_exp2(sv[bi][1][e] - mn);
+                    ls = ls + p0 + p1;
+                    float w0 = p0, w1 = p1;   // the P.V weights as the MMA will take them
+                    if constexpr (C::kI8) {
+                        // P times the block's V scale, rounded to fp16 here, so that
+                        // the bias sum uses exactly the weights the MMA multiplies
+                        const float2 r = __half22float2(__floats2half2_rn(p0 * vsc[bi], p1 * vsc[bi]));
+                        w0 = r.x;
+                        w1 = r.y;
+                        wsum += w0 + w1;
+                    }
+                    if (2 * tq + e < G) {   // P[head][token]
+                        pbuf[(2 * tq + e) * C::PS + kBlockSize * bi + gq] = w0;
+                        pbuf[(2 * tq + e) * C::PS + kBlockSize * bi + gq + 8] = w1;
+                    }
                 }
+                lsum[e] = ls;
+                if constexpr (C::kI8) pv[e] = fmaf(pv[e], alpha[e], wsum);
             }
             if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
@@ -660,33 +771,45 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
                     oa[i][2] *= alpha[0]; oa[i][3] *= alpha[1];
                 }
             }
-            load_v(vt, nv);
+            if constexpr (!C::kI8) load_v(vt, nv, 0);
             __syncwarp();
-            // P^T as the B operand: column gq = head gq, tokens 2tq, 2tq + 1 | + 8.
-            // P = hi + lo in two parts of the operand type (hi = rn(P), lo =
-            // rn(P - hi), the difference exact in fp32), so a weight in [0, 1]
-            // is off by at most 2^-18 (bf16): with one 16-bit P a two-token
-            // context would be off by up to 2^-9 |v|.
-            uint32_t ph[2] = {0u, 0u}, pl[2] = {0u, 0u};
-            if (gq < G) {
+            // P^T as the B operand: column gq = head gq, tokens 2tq, 2tq + 1 | + 8
+            // of each block. 16-bit caches: P = hi + lo in two parts of the
+            // operand type (hi = rn(P), lo = rn(P - hi), the difference exact in
+            // fp32), so a weight in [0, 1] is off by at most 2^-18 (bf16): with
+            // one 16-bit P a two-token context would be off by up to 2^-9 |v|.
+            // INT8: one fp16 part (already rounded above), off by at most 2^-11
+            // of the weight, i.e. 2^-11 max|v| on the output, far inside the
+            // INT8 bound.
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float2 f = *reinterpret_cast<const float2*>(pbuf + gq * kBlockSize + 2 * tq + 8 * k);
-                    ph[k] = pack2<MMT>(f.x, f.y);
-                    const float2 r = unpack2(MMT{}, ph[k]);
-                    pl[k] = pack2<MMT>(f.x - r.x, f.y - r.y);
+            for (int bi = 0; bi < C::UB; ++bi) {
+                if constexpr (C::kI8) load_v(vt, nv, bi);
+                uint32_t ph[2] = {0u, 0u}, pl[2] = {0u, 0u};
+                if (gq < G) {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 f = *reinterpret_cast<const float2*>(
+                            pbuf + gq * C::PS + kBlockSize * bi + 2 * tq + 8 * k);
+                        ph[k] = pack2<MMT>(f.x, f.y);
+                        if constexpr (!C::kI8) {
+                            const float2 r = unpack2(MMT{}, ph[k]);
+                            pl[k] = pack2<MMT>(f.x - r.x, f.y - r.y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < MT; ++i) mma16816<MMT>(oa[i], va[i], ph[0], ph[1]);
+                if constexpr (!C::kI8) {
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) mma16816<MMT>(oa[i], va[i], pl[0], pl[1]);
                 }
             }
-#pragma unroll
-            for (int i = 0; i < MT; ++i) mma16816<MMT>(oa[i], va[i], ph[0], ph[1]);
-#pragma unroll
-            for (int i = 0; i < MT; ++i) mma16816<MMT>(oa[i], va[i], pl[0], pl[1]);
         }
         // The stage goes back to the copy engine only after the math: releasing
         // it right after its reads (with V held in registers) measured slower.
         __syncwarp();
         if (u_issue < u1) {
-            issue(u_issue, s);
+            issue(u_issue, s, 0u);
             ++u_issue;
         }
     }
@@ -800,6 +923,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
 // ------------------------------------------------------------------- host ---
 struct Ops {
     int warp_bytes;
+    int warps;             // worker warps per CTA
     int max_ctas_per_sm;   // cap on the default worker count (0 = occupancy)
     cudaError_t (*prepare)(size_t smem);                        // smem attribute
     cudaError_t (*occupancy)(int* blocks, size_t smem);
@@ -817,10 +941,11 @@ struct Impl {
         cudaError_t e = prepare(smem);
         if (e != cudaSuccess) return e;
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            blocks, decode_split_kernel<KV, QT, D, G>, kThreads, smem);
+            blocks, decode_split_kernel<KV, QT, D, G>, Cfg<KV, D, G>::THREADS, smem);
     }
     static void split(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-        launch_pdl(decode_split_kernel<KV, QT, D, G>, dim3(grid), dim3(kThreads), smem, st, p);
+        launch_pdl(decode_split_kernel<KV, QT, D, G>, dim3(grid), dim3(Cfg<KV, D, G>::THREADS),
+                   smem, st, p);
     }
     static void combine(const CombineParams& c, int grid, cudaStream_t st) {
         launch_pdl(decode_combine_kernel<QT, D, G>, dim3(grid), dim3(kCombineThreads), 0, st, c);
@@ -828,10 +953,13 @@ struct Impl {
     // 16-bit caches at D = 128 default to 2 CTAs (8 worker warps) per SM
     // although 3 fit: on the GQA-8B workload the split kernel read 6.74 TB/s
     // with 8 warps per SM against 6.38 TB/s with 12 (same GPU, back to back),
-    // and g = 8, whose shared memory allows only 2, read 6.71 TB/s.
+    // and g = 8, whose shared memory allows only 2, read 6.71 TB/s. INT8
+    // (two-block units, 6-warp CTAs) keeps full occupancy: 12 warps per SM
+    // read 6.07 TB/s on the INT8 GQA-8B workload, 8 warps 4.2 TB/s.
     static constexpr int kCap = (Elem<KV>::bytes == 2 && D == 128) ? 2 : 0;
     static Ops ops() {
-        return Ops{Cfg<KV, D, G>::WARP_BYTES, kCap, prepare, occupancy, split, combine};
+        return Ops{Cfg<KV, D, G>::WARP_BYTES, Cfg<KV, D, G>::WARPS, kCap, prepare, occupancy,
+                   split, combine};
     }
 };
 
@@ -897,7 +1025,7 @@ pkv_status check_decode(const pkv_cache_desc* c, int batch, int hq, pkv_dtype q_
 }
 
 size_t split_smem(const Ops& o, int batch) {
-    return size_t(prefix_bytes(batch)) + size_t(kWarpsPerCta) * o.warp_bytes;
+    return size_t(prefix_bytes(batch)) + size_t(o.warps) * o.warp_bytes;
 }
 
 // Default worker warps on the current device for this configuration: the
@@ -908,7 +1036,7 @@ long long default_workers(const Ops& o, int batch) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (o.occupancy(&blocks, split_smem(o, batch)) != cudaSuccess || blocks <= 0) return 0;
     if (o.max_ctas_per_sm > 0 && blocks > o.max_ctas_per_sm) blocks = o.max_ctas_per_sm;
-    return (long long)sms * blocks * kWarpsPerCta;
+    return (long long)sms * blocks * o.warps;
 }
 
 pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q_dtype,
@@ -918,7 +1046,8 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
                       int32_t batch, int32_t hq, float softmax_scale, void* out, void* workspace,
                       size_t workspace_bytes, int32_t num_parts, uint32_t* dev_status,
                       cudaStream_t stream, const void* k_new = nullptr,
-                      const void* v_new = nullptr) {
+                      const void* v_new = nullptr, uint64_t wait_ns = kWaitLimitNs,
+                      int stall_worker = -1) {
     Ops ops;
     int G = 0;
     pkv_status s = check_decode(cache, batch, hq, q_dtype, &ops, &G);
@@ -962,7 +1091,9 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
         p.batch = batch; p.hq = hq; p.hkv = hkv; p.mb = mb; p.num_blocks = cache->num_blocks;
         p.workers = int(workers);
         p.qscale = softmax_scale * kLog2e;
-        const int grid = int((workers + kWarpsPerCta - 1) / kWarpsPerCta);
+        p.wait_ns = wait_ns;
+        p.stall_worker = stall_worker;
+        const int grid = int((workers + ops.warps - 1) / ops.warps);
         ops.split(p, grid, smem, stream);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
@@ -1125,4 +1256,21 @@ extern "C" pkv_status pkv_decode_attn_noalloc(const void* q, pkv_dtype q_dtype,
                       block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
                       softmax_scale, out, ws, kNoAllocScratchBytes, int32_t(workers), dev_status,
                       stream);
+}
+
+// ------------------------------------------------------------- test hook ---
+#include "../../include/pkv_testing.h"
+
+extern "C" pkv_status pkv_testing_decode_attn_stall(
+    const void* q, pkv_dtype q_dtype, const void* k_cache, const void* v_cache,
+    const float* k_scales, const float* v_scales, const pkv_cache_desc* cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t batch, int32_t num_q_heads, float softmax_scale, void* out, void* workspace,
+    size_t workspace_bytes, int32_t num_parts, uint64_t wait_limit_ns, int32_t stall_worker,
+    uint32_t* dev_status, cudaStream_t stream) {
+    if (wait_limit_ns > kWaitLimitNs || stall_worker < -1) return PKV_ERR_INVALID_ARG;
+    return run_decode(true, true, q, q_dtype, k_cache, v_cache, k_scales, v_scales, cache,
+                      block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                      softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status,
+                      stream, nullptr, nullptr, wait_limit_ns, stall_worker);
 }

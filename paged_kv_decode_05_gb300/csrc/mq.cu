@@ -49,6 +49,10 @@ struct MqParams {
     uint32_t* status;
     int batch, hq, hkv, mb, num_blocks, workers, tmax, max_q;
     float qscale;                // softmax_scale * log2(e)
+    uint64_t wait_ns;            // limit of each bounded wait
+    int stall_cta;               // test hook: this CTA's first unit (split kernel) or
+                                 // first chunk (tcgen05 kernel) expects 16 bytes no
+                                 // copy delivers, so its wait runs out (-1: none)
 };
 
 // Blocks the rows of row tile t can see: its last query sits at position
@@ -256,7 +260,7 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             const int n = __shfl_sync(kFull, cn, idx), L = __shfl_sync(kFull, cL, idx);
             const int blk = __shfl_sync(kFull, cblk, idx), cu = __shfl_sync(kFull, ccu, idx);
             if (u - u0 >= NS) {  // wait until every consumer released this stage
-                const bool ok = mbar_wait_bounded(smem_addr(&empty[s]), (parity >> s) & 1u, kMqWaitNs);
+                const bool ok = mbar_wait_bounded(smem_addr(&empty[s]), (parity >> s) & 1u, p.wait_ns);
                 parity ^= 1u << s;
                 if (!__all_sync(kFull, ok)) {   // records where it gave up: bit 9
                     if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT | 0x200u);
@@ -266,13 +270,14 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&full[s]);
                 const bool valid = unsigned(blk) < unsigned(p.num_blocks);
+                const uint32_t extra = (u == u0 && wk == p.stall_cta) ? 16u : 0u;
                 meta[2 * s] = make_int4(b, kvh, t, j);
                 // (n, L, cu_q[b], flags: bit 0 = block valid, bit 1 = first unit of a piece)
                 meta[2 * s + 1] = make_int4(n, L, cu, (valid ? 1 : 0) | ((u == u0 || j == 0) ? 2 : 0));
                 if (valid) {
                     const int y = (blk * p.hkv + kvh) * kBlockSize;
                     unsigned char* st = smem + s * C::STAGE;
-                    mbar_arrive_expect_tx(bar, C::STAGE);
+                    mbar_arrive_expect_tx(bar, C::STAGE + extra);
 #pragma unroll
                     for (int sub = 0; sub < C::NSUB; ++sub) {
                         tma_load_2d(smem_addr(st + sub * C::SUB), &tmk, 64 * sub, y, bar);
@@ -280,7 +285,8 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                     }
                 } else {
                     flag_status(p.status, PKV_DEV_BAD_BLOCK);
-                    mbar_arrive(bar);
+                    if (extra) mbar_arrive_expect_tx(bar, extra);
+                    else mbar_arrive(bar);
                 }
             }
         }
@@ -333,7 +339,7 @@ mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
     int s = 0;
     bool aborted = false;
     for (int u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1) {
-        const bool got = mbar_wait_bounded(smem_addr(&full[s]), (parity >> s) & 1u, kMqWaitNs);
+        const bool got = mbar_wait_bounded(smem_addr(&full[s]), (parity >> s) & 1u, p.wait_ns);
         parity ^= 1u << s;
         if (!__all_sync(kFull, got)) {          // records where it gave up: bit 8
             if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT | 0x100u);
@@ -668,7 +674,7 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 
     auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t role_bit) -> bool {
         if (misc[1]) return false;
-        const bool ok = mbar_wait_bounded(smem_addr(bar), parity, 2000000000ull);
+        const bool ok = mbar_wait_bounded(smem_addr(bar), parity, p.wait_ns);
         if (!ok) {
             misc[1] = 1u;
             flag_status(p.status, PKV_DEV_TIMEOUT | role_bit);
@@ -679,6 +685,7 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     if (warp == 0) {
         // ------------------------------------------------------ producer ---
         if (lane == 0) {
+            int issued = 0;
             for (int c = 0; c < nch; ++c) {
                 const int st = c % kTcStages;
                 if (c >= kTcStages && !wait(&kv_empty[st], ((c / kTcStages) - 1) & 1, 0x400u)) break;
@@ -701,8 +708,11 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                 }
                 smask[st] = mask;
                 const uint32_t bar = smem_addr(&kv_full[st]);
-                if (nl) mbar_arrive_expect_tx(bar, uint32_t(nl * 2 * C::NH * kBlockSize * 128));
+                const uint32_t extra = (c == 0 && unit == p.stall_cta) ? 16u : 0u;
+                if (nl || extra)
+                    mbar_arrive_expect_tx(bar, uint32_t(nl * 2 * C::NH * kBlockSize * 128) + extra);
                 else mbar_arrive(bar);
+                ++issued;
                 unsigned char* sk = smem + C::OFF_KV + st * C::KV_STAGE;
 #pragma unroll
                 for (int jj = 0; jj < kTcChunk / kBlockSize; ++jj) {
@@ -716,6 +726,12 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                     }
                 }
             }
+            // After an abort, let the copies of the last chunks issued land
+            // (bounded) before the CTA may exit.
+            if (misc[1])
+                for (int c = max(0, issued - kTcStages); c < issued; ++c)
+                    mbar_wait_bounded(smem_addr(&kv_full[c % kTcStages]), (c / kTcStages) & 1,
+                                      p.wait_ns);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer ---
@@ -1175,15 +1191,17 @@ extern "C" size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_hea
     return pl.ws_total;
 }
 
-extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
-                                          int32_t max_q_len, const void* k_cache,
-                                          const void* v_cache, const pkv_cache_desc* cache,
-                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                          const int32_t* context_lens, int32_t batch,
-                                          int32_t num_q_heads, float softmax_scale, void* out,
-                                          void* workspace, size_t workspace_bytes,
-                                          int32_t num_parts, uint32_t* dev_status,
-                                          cudaStream_t stream) {
+namespace {
+
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+
+pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
+                          int32_t max_q_len, const void* k_cache, const void* v_cache,
+                          const pkv_cache_desc* cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                          int32_t num_q_heads, float softmax_scale, void* out, void* workspace,
+                          size_t workspace_bytes, int32_t num_parts, uint32_t* dev_status,
+                          cudaStream_t stream, uint64_t wait_ns, int stall_cta) {
     MqPlan pl;
     pkv_status s = mq_plan(cache, batch, num_q_heads, max_q_len, q_dtype, num_parts, &pl);
     if (s != PKV_OK) return s;
@@ -1221,6 +1239,8 @@ extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, cons
         p.tmax = int(((long long)max_q_len * pl.G + kTcRows - 1) / kTcRows);
         p.max_q = max_q_len;
         p.qscale = softmax_scale * kMqLog2e;
+        p.wait_ns = wait_ns < kTcWaitNs ? wait_ns : kTcWaitNs;
+        p.stall_cta = stall_cta;
         const long long grid = (long long)batch * p.hkv * p.tmax;
         if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
         if (tc(tk, tv, p, int(grid), stream) != cudaSuccess) return PKV_ERR_CUDA;
@@ -1238,6 +1258,8 @@ extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, cons
     p.num_blocks = cache->num_blocks; p.workers = int(pl.workers); p.tmax = pl.tmax;
     p.max_q = max_q_len;
     p.qscale = softmax_scale * kMqLog2e;
+    p.wait_ns = wait_ns;
+    p.stall_cta = stall_cta;
     if (pl.ops.prepare(pl.smem) != cudaSuccess) return PKV_ERR_CUDA;
     if (pl.ops.split(tk, tv, p, int(pl.workers), pl.smem, stream) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -1250,4 +1272,37 @@ extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, cons
     if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
     if (pl.ops.combine(cb, int(grid), stream) != cudaSuccess) return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
+                                          int32_t max_q_len, const void* k_cache,
+                                          const void* v_cache, const pkv_cache_desc* cache,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t batch,
+                                          int32_t num_q_heads, float softmax_scale, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t num_parts, uint32_t* dev_status,
+                                          cudaStream_t stream) {
+    return run_multiquery(q, q_dtype, cu_q, max_q_len, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, batch, num_q_heads, softmax_scale, out,
+                          workspace, workspace_bytes, num_parts, dev_status, stream, kMqWaitNs,
+                          -1);
+}
+
+// ------------------------------------------------------------- test hook ---
+#include "../../include/pkv_testing.h"
+
+extern "C" pkv_status pkv_testing_multiquery_attn_stall(
+    const void* q, pkv_dtype q_dtype, const int32_t* cu_q, int32_t max_q_len, const void* k_cache,
+    const void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+    float softmax_scale, void* out, void* workspace, size_t workspace_bytes, int32_t num_parts,
+    uint64_t wait_limit_ns, int32_t stall_cta, uint32_t* dev_status, cudaStream_t stream) {
+    if (wait_limit_ns > kMqWaitNs || stall_cta < -1) return PKV_ERR_INVALID_ARG;
+    return run_multiquery(q, q_dtype, cu_q, max_q_len, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, batch, num_q_heads, softmax_scale, out,
+                          workspace, workspace_bytes, num_parts, dev_status, stream, wait_limit_ns,
+                          stall_cta);
 }

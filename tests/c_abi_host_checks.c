@@ -112,6 +112,23 @@ int main(void) {
     CHECK(pkv_copy_blocks(fake, fake, NULL, NULL, &i8, fake, fake, 3, NULL, NULL) ==
           PKV_ERR_INVALID_ARG);                                     /* INT8 needs scales */
 
+    /* merge of partial states */
+    {
+        const float *ff = (const float *)fake;
+        CHECK(pkv_merge_states(ff, ff, ff, 8, fake, 0, 4, 128, PKV_BF16, fake, NULL, NULL, NULL,
+                               NULL) == PKV_OK);                    /* no rows */
+        CHECK(pkv_merge_states(ff, ff, ff, 8, fake, 2, 4, 126, PKV_BF16, fake, NULL, NULL, NULL,
+                               NULL) == PKV_ERR_INVALID_ARG);       /* head_dim % 4 */
+        CHECK(pkv_merge_states(ff, ff, ff, 8, fake, 2, 4, 1024, PKV_BF16, fake, NULL, NULL, NULL,
+                               NULL) == PKV_ERR_UNSUPPORTED);       /* head_dim > 512 */
+        CHECK(pkv_merge_states(ff, ff, ff, 8, fake, 2, 4, 128, PKV_I8, fake, NULL, NULL, NULL,
+                               NULL) == PKV_ERR_INVALID_ARG);       /* out dtype */
+        CHECK(pkv_merge_states(ff, ff, (const float *)fake8, 8, fake, 2, 4, 128, PKV_BF16, fake,
+                               NULL, NULL, NULL, NULL) == PKV_ERR_INVALID_ARG);   /* o misaligned */
+        CHECK(pkv_merge_states(NULL, ff, ff, 8, fake, 2, 4, 128, PKV_BF16, fake, NULL, NULL, NULL,
+                               NULL) == PKV_ERR_INVALID_ARG);       /* m missing */
+    }
+
     if (failures) {
         printf("%d check(s) failed\n", failures);
         return 1;

@@ -13,7 +13,8 @@ import pytest
 from paged_kv_decode_05_gb300 import binding as B
 from paged_kv_decode_05_gb300.build import build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -23,7 +24,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
 

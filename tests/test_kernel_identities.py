@@ -54,3 +54,31 @@ def test_p_split_into_two_16bit_parts():
     assert rel16[normal].max() <= 2.0 ** -22
     # below fp16's normal range the second part still bounds the absolute error
     assert (np.abs((hi16.astype(np.float64) + lo16) - p)[~normal]).max() <= 2.0 ** -25
+
+
+def test_int8_single_fp16_weight_error_bound():
+    """INT8 caches: the P.V product takes each weight as one fp16 value
+    w = rn16(P * s_v) (s_v the block's V scale, P in [0, 1] in fp32) and the
+    code carrier's 1152 bias is removed with the sum of those same w, so the
+    bias cancels and the output error is that of the rounded weights alone:
+    |out - exact| <= 2^-11 max|v| (fp16 rounds normal values within 2^-11
+    relative; weights below fp16's normal range are off by at most 2^-25
+    absolute). Checked in float64 on short contexts, where single weights are
+    largest, and far inside the INT8 bound of 2e-2 for |v| up to ~5."""
+    rng = np.random.default_rng(3)
+    worst = 0.0
+    for _ in range(3000):
+        n = int(rng.integers(1, 40))
+        codes = rng.integers(-127, 128, n).astype(np.float64)
+        sv = np.float32(rng.uniform(0.002, 0.05))
+        s = rng.normal(0, 3, n).astype(np.float32)
+        p = np.exp2((s - s.max()) * np.float32(1.4426950408889634)).astype(np.float32)
+        w = (p * sv).astype(np.float32).astype(np.float16).astype(np.float64)
+        l = float(p.astype(np.float64).sum())
+        got = (np.sum(w * (1152.0 + codes)) - 1152.0 * w.sum()) / l
+        want = float(np.sum(p.astype(np.float64) * codes * np.float64(sv)) / l)
+        vmax = float(np.abs(codes).max() * np.float64(sv))
+        err = abs(got - want)
+        assert err <= 2.0 ** -11 * vmax + 2.0 ** -25 * n * 127 * float(sv) / l + 1e-12
+        worst = max(worst, err)
+    assert worst < 2e-2 / 8

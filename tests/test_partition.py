@@ -1,7 +1,10 @@
 """The split kernel's work partition, checked by brute force on the CPU.
 
-The decode split cuts the unit stream (sequence b, kv head, block j) into W
-equal contiguous ranges; a (b, kv head) segment crossing ranges leaves one
+The decode split cuts the unit stream (sequence b, kv head, unit j) into W
+equal contiguous ranges (a unit is one 16-token block for fp16 / bf16 caches
+and two consecutive blocks of the sequence for INT8 caches, so a sequence of
+L tokens has ceil(L / 16) or ceil(L / 32) units per kv head; the partition is
+the same either way); a (b, kv head) segment crossing ranges leaves one
 partial state per range at slot ``segment + worker``, and the combine finds a
 segment's ranges as ``worker_of(first unit) .. worker_of(last unit)`` minus
 empty ranges. This restates that index arithmetic in Python and checks, for
