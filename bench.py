@@ -325,7 +325,7 @@ def _gpu_state(w, device):
         st["k_scales"] = torch.zeros(shape[:2], dtype=torch.float32, device=device)
         st["v_scales"] = torch.zeros(shape[:2], dtype=torch.float32, device=device)
         n = B.pkv_append_workspace_size(st["k_cache"])
-        st["append_ws"] = torch.empty(n, dtype=torch.uint8, device=device)
+        st["append_ws"] = torch.zeros(n, dtype=torch.uint8, device=device)   # zeroed once
     else:
         dt = torch.bfloat16 if cfg.kv_dtype == "bf16" else torch.float16
         st["k_cache"] = torch.zeros(shape, dtype=dt, device=device)
@@ -427,7 +427,7 @@ def run_native(args):
                      dtype=torch.uint8, device=device)
     alg = algorithmic_bytes(cfg, w.context_lens)
     st["fused"] = (not args.unfused) and cfg.kv_dtype != "i8"
-    launches_per_step = 2 if st["fused"] else (6 if cfg.kv_dtype == "i8" else 3)
+    launches_per_step = 2 if st["fused"] else (4 if cfg.kv_dtype == "i8" else 3)
     K, W = args.steps, args.warmup
 
     props = torch.cuda.get_device_properties(device)

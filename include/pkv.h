@@ -32,9 +32,10 @@
  *
  * Ownership and synchronisation: every pointer argument is caller-owned
  * DEVICE memory, except the pkv_cache_desc pointer (host). The library
- * allocates nothing. Between calls it keeps only two lookups, each made once:
- * the driver's tensor-map encoder (pkv_multiquery_attn) and, per device, the
- * address of pkv_decode_attn_noalloc's built-in scratch array. Every call only
+ * allocates nothing. Between calls it keeps only lookups, each made once:
+ * two driver entry points (the tensor-map encoder of pkv_multiquery_attn and
+ * the current-context query of pkv_decode_attn_noalloc) and, per CUDA
+ * context, the address of pkv_decode_attn_noalloc's built-in scratch array. Every call only
  * enqueues kernels on `stream` and returns; inputs must stay valid until the
  * stream has executed them.
  *
@@ -109,8 +110,11 @@ const char *pkv_status_string(pkv_status s);
  * every stored code q of the tile becomes rne((float)q * s_o / s) (fp32, left
  * to right). New codes are clamp(rne(x / s), -127, 127), or 0 when s == 0.
  * k_scales / v_scales must start at 0 for never-written blocks. The call needs
- * a workspace of pkv_append_workspace_size(cache) bytes (no initial contents
- * required; 16-byte aligned). Inputs must be finite.
+ * a workspace of pkv_append_workspace_size(cache) bytes (80 bytes per
+ * (block, kv_head) tile; 16-byte aligned), zero-filled before its first use:
+ * each call leaves it zero-filled again, so one workspace serves every later
+ * call on the same cache (calls that overlap on the GPU must not share it).
+ * Inputs must be finite.
  *
  * Alignment: k_new, v_new, k_cache, v_cache 16-byte aligned.
  * ------------------------------------------------------------------------ */
@@ -332,9 +336,11 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, float *k_scales, float 
  * - Calls that need more scratch than that (pkv_decode_workspace_size for
  *   the same batch, num_q_heads, cache and num_parts) return
  *   PKV_ERR_WORKSPACE and launch nothing.
- * - The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any stream
- *   capture.
+ * - The array's device address belongs to a CUDA context: the first call in
+ *   each context (e.g. the device's primary context, which the CUDA runtime
+ *   uses) looks it up once, with that device current; later calls in the same
+ *   context reuse it. Make that first call before any stream capture. Up to
+ *   64 (device, context) pairs per process; more return PKV_ERR_UNSUPPORTED.
  * - All calls share the one array and it keeps the last call's contents;
  *   nothing in it needs to start at zero, since each call rewrites every part
  *   it later reads. Calls whose work overlaps on the GPU (other streams, other

@@ -8,13 +8,15 @@
 // (paged-inference-engine overview, "paged INT8 KV storage").
 //
 // fp16/bf16: one 16-byte vector per thread, a bit copy.
-// INT8: four stream-ordered kernels over (token, kv_head) warps, so that every
+// INT8: two stream-ordered kernels over (token, kv_head) warps, so that every
 // (block, kv_head) tile sees all of a call's new rows before its scale is set:
-//   clear  -> zero the tile's scratch (absmax of K, of V, owner claim)
-//   absmax -> atomicMax of each row's |x| max; atomicMax owner claim N - n
-//   scale  -> the owning warp sets the tile scale, requantising stored codes
-//             when the scale grows
-//   quant  -> every warp encodes its row with the tile's final scale
+//   gather -> per tile: atomicMax of each new row's |x| max (K and V), an
+//             owner claim (the call's first token in the tile), the set of
+//             rows the call writes and each such row's token index
+//   settle -> the owning warp alone sets the tile's scale, requantises the
+//             stored codes when the scale grows, encodes every new row of
+//             the tile under the final scale and clears the tile's scratch,
+//             so the workspace is zero again for the next call
 #include "common.cuh"
 
 namespace pkv {
@@ -51,6 +53,13 @@ __global__ void append_copy_kernel(const uint4* __restrict__ k_new, const uint4*
 }
 
 // ---------------------------------------------------------------- INT8 ---
+// Per-tile scratch: absmax bits of K and of V, the owner claim N - n of the
+// call's first token in the tile, and the mask of rows the call writes; all
+// zero between calls. Beside it, the token index of each row the call writes.
+struct TileScratch {
+    uint32_t amax_k, amax_v, owner, rows;
+};
+
 struct I8Args {
     const void* k_new;
     const void* v_new;
@@ -59,9 +68,8 @@ struct I8Args {
     int8_t* v_cache;
     float* k_scales;
     float* v_scales;
-    uint32_t* amax_k;     // scratch [num_blocks * hkv]
-    uint32_t* amax_v;
-    uint32_t* owner;
+    TileScratch* tiles;   // [num_blocks * hkv]
+    int32_t* row_tok;     // [num_blocks * hkv * 16]
     uint32_t* status;
     int n_tokens;
     int hkv;
@@ -98,7 +106,8 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-__global__ void i8_clear_kernel(I8Args a) {
+template <typename S, int D>
+__global__ void i8_gather_kernel(I8Args a) {
     griddep_wait();
     griddep_launch_dependents();
     const long long items = (long long)a.n_tokens * a.hkv;
@@ -107,23 +116,6 @@ __global__ void i8_clear_kernel(I8Args a) {
         long long n;
         int row;
         const long long t = item_tile(a, it, &n, &row, true);
-        if (t < 0 || (threadIdx.x & 31)) continue;
-        a.amax_k[t] = 0u;
-        a.amax_v[t] = 0u;
-        a.owner[t] = 0u;
-    }
-}
-
-template <typename S, int D>
-__global__ void i8_absmax_kernel(I8Args a) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const long long items = (long long)a.n_tokens * a.hkv;
-    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
-         it += ((long long)gridDim.x * blockDim.x) >> 5) {
-        long long n;
-        int row;
-        const long long t = item_tile(a, it, &n, &row, false);
         if (t < 0) continue;
         float xk[D / 32], xv[D / 32];
         load_row<S, D>(a.k_new, it * D, xk);
@@ -137,54 +129,28 @@ __global__ void i8_absmax_kernel(I8Args a) {
         mk = warp_max(mk);
         mv = warp_max(mv);
         if ((threadIdx.x & 31) == 0) {
+            TileScratch* ts = a.tiles + t;
             // non-negative floats order like their bit patterns
-            atomicMax(&a.amax_k[t], __float_as_uint(mk));
-            atomicMax(&a.amax_v[t], __float_as_uint(mv));
-            atomicMax(&a.owner[t], uint32_t(a.n_tokens - n));
+            atomicMax(&ts->amax_k, __float_as_uint(mk));
+            atomicMax(&ts->amax_v, __float_as_uint(mv));
+            atomicMax(&ts->owner, uint32_t(a.n_tokens - n));
+            atomicOr(&ts->rows, 1u << row);
+            a.row_tok[t * kBlockSize + row] = int32_t(n);
         }
     }
 }
 
-// Settle one (block, kv_head) tile's scale; requantise its codes on growth.
-__device__ __forceinline__ void settle_tile(int8_t* cache, float* scales, uint32_t amax_bits,
-                                           long long t, int D) {
+// The tile's scale from the call's absmax and the stored scale s_o (0 = never
+// written): s_c = a / 127 (IEEE division); s = s_c if s_o == 0, s_o if
+// s_c <= s_o, else s_c (the tile's stored codes are then requantised).
+__device__ __forceinline__ float settle_scale(uint32_t amax_bits, float s_o, bool* grow) {
     const float s_c = __fdiv_rn(__uint_as_float(amax_bits), 127.0f);
-    const float s_o = scales[t];
-    float s = s_c;
-    bool grow = false;
-    if (s_o != 0.f) {
-        if (s_c <= s_o) s = s_o;
-        else grow = true;
-    }
-    if (grow) {
-        uint32_t* words = reinterpret_cast<uint32_t*>(cache + t * kBlockSize * D);
-        const int n_words = kBlockSize * D / 4;
-        for (int w = threadIdx.x & 31; w < n_words; w += 32) {
-            words[w] = requant_word(words[w], s_o, s);
-        }
-    }
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) scales[t] = s;
-}
-
-template <int D>
-__global__ void i8_scale_kernel(I8Args a) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const long long items = (long long)a.n_tokens * a.hkv;
-    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
-         it += ((long long)gridDim.x * blockDim.x) >> 5) {
-        long long n;
-        int row;
-        const long long t = item_tile(a, it, &n, &row, false);
-        if (t < 0 || a.owner[t] != uint32_t(a.n_tokens - n)) continue;
-        settle_tile(a.k_cache, a.k_scales, a.amax_k[t], t, D);
-        settle_tile(a.v_cache, a.v_scales, a.amax_v[t], t, D);
-    }
+    *grow = (s_o != 0.f) && !(s_c <= s_o);
+    return (s_o != 0.f && s_c <= s_o) ? s_o : s_c;
 }
 
 template <typename S, int D>
-__global__ void i8_quant_kernel(I8Args a) {
+__global__ void i8_settle_kernel(I8Args a) {
     griddep_wait();
     griddep_launch_dependents();
     constexpr int EPL = D / 32;
@@ -196,20 +162,41 @@ __global__ void i8_quant_kernel(I8Args a) {
         int row;
         const long long t = item_tile(a, it, &n, &row, false);
         if (t < 0) continue;
-        const long long dst = (t * kBlockSize + row) * D + lane * EPL;
+        TileScratch* ts = a.tiles + t;
+        const TileScratch sc = *ts;
+        if (sc.owner != uint32_t(a.n_tokens - n)) continue;   // one warp per tile
+        const int kvh = int(t % a.hkv);
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
-            float x[EPL];
-            load_row<S, D>(kv ? a.v_new : a.k_new, it * D, x);
-            const float s = (kv ? a.v_scales : a.k_scales)[t];
-            uint32_t packed = 0;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e)
-                packed |= (uint32_t(quant_code(x[e], s)) & 0xffu) << (8 * e);
             int8_t* cache = kv ? a.v_cache : a.k_cache;
-            if (EPL == 4) *reinterpret_cast<uint32_t*>(cache + dst) = packed;
-            else *reinterpret_cast<uint16_t*>(cache + dst) = uint16_t(packed);
+            float* scales = kv ? a.v_scales : a.k_scales;
+            const float s_o = scales[t];
+            bool grow;
+            const float s = settle_scale(kv ? sc.amax_v : sc.amax_k, s_o, &grow);
+            if (grow) {   // every stored code re-expressed under the grown scale
+                uint32_t* words = reinterpret_cast<uint32_t*>(cache + t * kBlockSize * D);
+                for (int w = lane; w < kBlockSize * D / 4; w += 32)
+                    words[w] = requant_word(words[w], s_o, s);
+            }
+            __syncwarp();
+            // the call's new rows of the tile, under the final scale
+            for (uint32_t m = sc.rows; m; m &= m - 1) {
+                const int r = __ffs(m) - 1;
+                const long long src = ((long long)a.row_tok[t * kBlockSize + r] * a.hkv + kvh) * D;
+                float x[EPL];
+                load_row<S, D>(kv ? a.v_new : a.k_new, src, x);
+                uint32_t packed = 0;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e)
+                    packed |= (uint32_t(quant_code(x[e], s)) & 0xffu) << (8 * e);
+                const long long dst = (t * kBlockSize + r) * D + lane * EPL;
+                if (EPL == 4) *reinterpret_cast<uint32_t*>(cache + dst) = packed;
+                else *reinterpret_cast<uint16_t*>(cache + dst) = uint16_t(packed);
+            }
+            if (lane == 0) scales[t] = s;
         }
+        __syncwarp();
+        if (lane == 0) *ts = TileScratch{0u, 0u, 0u, 0u};   // zero again for the next call
     }
 }
 
@@ -235,10 +222,8 @@ template <typename S, int D>
 void launch_i8(const I8Args& a, cudaStream_t st) {
     const long long items = (long long)a.n_tokens * a.hkv;
     const int g = grid_for(items, kWarps, 1 << 16);
-    launch_pdl(i8_clear_kernel, dim3(g), dim3(kThreads), 0, st, a);
-    launch_pdl(i8_absmax_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
-    launch_pdl(i8_scale_kernel<D>, dim3(g), dim3(kThreads), 0, st, a);
-    launch_pdl(i8_quant_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
+    launch_pdl(i8_gather_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
+    launch_pdl(i8_settle_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
 }
 
 }  // namespace
@@ -250,7 +235,7 @@ extern "C" size_t pkv_append_workspace_size(const pkv_cache_desc* cache) {
     if (check_cache(cache) != PKV_OK) return 0;
     if (cache->kv_dtype != PKV_I8) return 0;
     const size_t tiles = size_t(cache->num_blocks) * size_t(cache->num_kv_heads);
-    return 3 * tiles * sizeof(uint32_t);
+    return tiles * (sizeof(TileScratch) + kBlockSize * sizeof(int32_t));
 }
 
 extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, pkv_dtype src_dtype,
@@ -286,10 +271,10 @@ extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, pkv_dtype
         const size_t need = pkv_append_workspace_size(cache);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PKV_ERR_WORKSPACE;
         const size_t tiles = size_t(cache->num_blocks) * size_t(hkv);
-        uint32_t* ws = static_cast<uint32_t*>(workspace);
+        TileScratch* ws = static_cast<TileScratch*>(workspace);
         I8Args a{k_new, v_new, slot_mapping, static_cast<int8_t*>(k_cache),
-                 static_cast<int8_t*>(v_cache), k_scales, v_scales, ws, ws + tiles,
-                 ws + 2 * tiles, dev_status, num_tokens, hkv, pool_slots};
+                 static_cast<int8_t*>(v_cache), k_scales, v_scales, ws,
+                 reinterpret_cast<int32_t*>(ws + tiles), dev_status, num_tokens, hkv, pool_slots};
         if (src_dtype == PKV_BF16) {
             if (D == 128) launch_i8<BF16, 128>(a, stream); else launch_i8<BF16, 64>(a, stream);
         } else {

@@ -1197,33 +1197,70 @@ extern "C" pkv_status pkv_decode_combine(const pkv_cache_desc* cache, int32_t ba
 // ------------------------------------------------ no-allocation variant ---
 // pkv_decode_attn_noalloc: the same split + combine, with the scratch taken
 // from a fixed array compiled into this file instead of a caller workspace.
+#include <cuda.h>
+
 #include <mutex>
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxContexts = 64;
 
 // Device-resident scratch. In host code this name is only a stand-in; the
 // device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's address belongs to a CUDA context (each context that loads the
+// module has its own copy), so it is cached per (device, context).
+struct NoAllocEntry {
+    int device;
+    CUcontext ctx;
+    void* ptr;
+};
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+NoAllocEntry g_noalloc[kNoAllocMaxContexts];
+int g_noalloc_n = 0;
 
-// Once per device, with that device current: resolve the array's address.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static std::once_flag once;
+    static CtxGetCurrentFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    });
+    return fn;
+}
+
+// Once per (device, context), with that device and context current: resolve
+// the array's address. Later calls in the same context reuse it.
 pkv_status noalloc_scratch(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return PKV_ERR_UNSUPPORTED;
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (!get) return PKV_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return PKV_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    for (int i = 0; ctx != nullptr && i < g_noalloc_n; ++i)
+        if (g_noalloc[i].device == dev && g_noalloc[i].ctx == ctx) {
+            *out = g_noalloc[i].ptr;
+            return PKV_OK;
+        }
+    if (g_noalloc_n == kNoAllocMaxContexts) return PKV_ERR_UNSUPPORTED;
+    // Resolving the address also makes the device's primary context current
+    // if no context was yet, so the context is read again afterwards.
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PKV_ERR_CUDA;
+    g_noalloc[g_noalloc_n++] = NoAllocEntry{dev, ctx, p};
+    *out = p;
     return PKV_OK;
 }
 

@@ -58,7 +58,7 @@ class GpuCase:
             self.k_scales = torch.zeros(shape[:2], dtype=torch.float32, device="cuda")
             self.v_scales = torch.zeros(shape[:2], dtype=torch.float32, device="cuda")
             nbytes = B.pkv_append_workspace_size(self.k_cache)
-            self.append_ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+            self.append_ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda")
         else:
             dt = torch_dtype(cfg.kv_dtype)
             fill = NAN16[cfg.kv_dtype] if stale == "nan" else 0

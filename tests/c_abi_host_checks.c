@@ -50,7 +50,7 @@ int main(void) {
 
     /* append: scratch sizes, nothing to do, rejected arguments */
     CHECK(pkv_append_workspace_size(&bf16) == 0);
-    CHECK(pkv_append_workspace_size(&i8) == 3u * 64u * 8u * 4u);
+    CHECK(pkv_append_workspace_size(&i8) == 80u * 64u * 8u);   /* 80 bytes per tile */
     CHECK(pkv_append_workspace_size(&d96) == 0);
     CHECK(pkv_append(NULL, NULL, PKV_BF16, 0, NULL, NULL, NULL, NULL, NULL, &bf16, NULL, 0,
                      NULL, NULL) == PKV_OK);

@@ -68,7 +68,7 @@ def test_append_host_validation(lib):
                           ctypes.byref(d96), None, 0, None, None) == 2
     d8 = desc(dt=B.PKV_I8)
     need = lib.pkv_append_workspace_size(ctypes.byref(d8))
-    assert need == 3 * 8 * 2 * 4
+    assert need == 80 * 8 * 2          # 80 bytes per (block, kv head) tile
     assert lib.pkv_append(fake, fake, B.PKV_BF16, 4, fake, fake, fake, fake, fake,
                           ctypes.byref(d8), fake, need - 4, None, None) == 3  # workspace
     assert lib.pkv_append(fake, fake, B.PKV_BF16, 4, fake, fake, fake, None, fake,
