@@ -109,17 +109,19 @@ def load_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash(source: str = "decode.cu") -> str:
+def kernel_source_hash(source="decode.cu") -> str:
     """sha256 (first 16 hex digits) of the device code a kernel is built from:
-    ``source`` up to its host-code marker line (``// ---- ... host ---``),
-    followed by common.cuh. Host-side edits below the marker leave it alone."""
+    each file of ``source`` (a name or a tuple of names) up to its host-code
+    marker line (``// ---- ... host ---``), followed by common.cuh. Host-side
+    edits below the marker leave it alone."""
     import hashlib
     csrc = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc")
-    with open(os.path.join(csrc, source), "rb") as f:
-        text = f.read()
-    m = re.search(rb"^// -+ host -+$", text, re.M)
-    if m:
-        text = text[:m.start()]
+    text = b""
+    for name in ((source,) if isinstance(source, str) else tuple(source)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            part = f.read()
+        m = re.search(rb"^// -+ host -+$", part, re.M)
+        text += part[:m.start()] if m else part
     with open(os.path.join(csrc, "common.cuh"), "rb") as f:
         text += f.read()
     return hashlib.sha256(text).hexdigest()[:16]
@@ -726,7 +728,7 @@ def run_multiquery(args):
             ev[1].record()
         B.pkv_multiquery_attn(st["q"], cu, nq, st["k_cache"], st["v_cache"], st["block_tables"],
                               st["context_lens"], cfg.softmax_scale, out, ws, args.num_parts,
-                              st["status"])
+                              st["status"], k_scales=st["k_scales"], v_scales=st["v_scales"])
         if ev is not None:
             ev[2].record()
 
@@ -765,14 +767,16 @@ def run_multiquery(args):
     tpeak, tsrc = load_tensor_peak()
     gbs = alg / (attn_ms / 1e3) / 1e9
     tflops = flops / (attn_ms / 1e3) / 1e12
-    # The library's dispatch rule: runs that fill 128-row tiles (q_len x the
-    # group size) take the tcgen05 kernel, one launch; shorter runs the
-    # mma.sync split kernel and its combine, two launches. Plus the append.
+    # The library's dispatch rule: runs over fp16 / bf16 caches that fill
+    # 128-row tiles (q_len x the group size) take the tcgen05 kernel, one
+    # launch; shorter runs and INT8 caches the mma.sync split kernel and its
+    # combine, two launches. Plus the append (two kernels for INT8).
     g = cfg.num_q_heads // cfg.num_kv_heads
-    tc = nq * g >= 128
+    tc = nq * g >= 128 and cfg.kv_dtype != "i8"
     kernel = "mq_tc_kernel" if tc else "mq_split_kernel"
-    launches = 2 if tc else 3
-    traffic = recorded_traffic(kernel, args.config, "mq.cu")
+    launches = (1 if tc else 2) + (2 if cfg.kv_dtype == "i8" else 1)
+    traffic = recorded_traffic(kernel, args.config,
+                               ("mq_split.cuh", "mq.cu") if tc else ("mq_split.cuh",))
     # Bound: the workload's FLOP/byte against the machine balance (measured
     # tensor peak / measured HBM bandwidth). Long prefill chunks are dense
     # contractions; verification of a few draft tokens streams the cache.

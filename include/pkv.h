@@ -267,29 +267,34 @@ pkv_status pkv_merge_states(const float *part_m, const float *part_l, const floa
  * a continuous batch (mini-inference-engine overview). n_b = 1 everywhere is
  * decode attention.
  *
- * q, out: [cu_q[batch], num_q_heads, head_dim], same dtype as the cache
- * (PKV_F16 or PKV_BF16; INT8 caches are not supported here). cu_q: device
- * int32 [batch+1], non-decreasing. max_q_len bounds every n_b; a sequence
- * with n_b > max_q_len, n_b > L_b or L_b beyond its table is flagged
- * PKV_DEV_BAD_LENGTH and its rows are not written. The g = num_q_heads /
- * num_kv_heads query heads of each KV head and the n_b queries form the rows
- * of a tensor-core tile. Supported: head_dim 64 or 128, g in {1, 2, 4},
- * batch <= 4096. Workspace: pkv_multiquery_workspace_size with the same
- * batch, num_q_heads, max_q_len, cache and num_parts (0 = one range per
- * resident CTA); 256-byte aligned. Caches 16-byte aligned.
- * Two kernels serve the call: when max_q_len * g >= 128 (a prefill chunk)
- * and q, out are 16-byte aligned, a tcgen05 / tensor-memory kernel with one
- * CTA per (sequence, kv head, 128-row tile) and no split (num_parts and the
- * workspace are then not used, but are still checked); otherwise an
- * mma.sync kernel whose stream of units is cut into num_parts ranges and
- * merged by a combine kernel through the workspace. Both compute the same
- * causal attention within the same tolerance.
+ * q, out: [cu_q[batch], num_q_heads, head_dim]. fp16 / bf16 caches: q in
+ * the cache's dtype; INT8 caches: q PKV_F16 or PKV_BF16 (16-byte aligned),
+ * k_scales / v_scales as for pkv_decode_attn (NULL for 16-bit caches), values
+ * dequantised as code * scale. cu_q: device int32 [batch+1], non-decreasing.
+ * max_q_len bounds every n_b; a sequence with n_b > max_q_len, n_b > L_b or
+ * L_b beyond its table is flagged PKV_DEV_BAD_LENGTH and its rows are not
+ * written. The g = num_q_heads / num_kv_heads query heads of each KV head
+ * and the n_b queries form the rows of a tensor-core tile. Supported:
+ * head_dim 64 or 128, g in {1, 2, 4, 8}, batch <= 4096. Workspace:
+ * pkv_multiquery_workspace_size with the same batch, num_q_heads, max_q_len,
+ * cache and num_parts (0 = one range per resident CTA); 256-byte aligned.
+ * Caches 16-byte aligned.
+ * Two kernels serve the call: for fp16 / bf16 caches, when max_q_len * g >=
+ * 128 (a prefill chunk) and q, out are 16-byte aligned, a tcgen05 /
+ * tensor-memory kernel with one CTA per (sequence, kv head, 128-row tile)
+ * and no split (num_parts and the workspace are then not used, but are still
+ * checked); otherwise, and for every INT8 cache, an mma.sync kernel whose
+ * stream of units is cut into num_parts ranges and merged by a combine
+ * kernel through the workspace. Both compute the same causal attention
+ * within the same tolerance (INT8: within 2e-2 of attention over the
+ * dequantised cache).
  * ------------------------------------------------------------------------ */
 size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_q_len,
                                      const pkv_cache_desc *cache, int32_t num_parts);
 
 pkv_status pkv_multiquery_attn(const void *q, pkv_dtype q_dtype, const int32_t *cu_q,
                                int32_t max_q_len, const void *k_cache, const void *v_cache,
+                               const float *k_scales, const float *v_scales,
                                const pkv_cache_desc *cache, const int32_t *block_tables,
                                int32_t max_blocks_per_seq, const int32_t *context_lens,
                                int32_t batch, int32_t num_q_heads, float softmax_scale,

@@ -54,6 +54,7 @@ pkv_status pkv_testing_decode_attn_stall(const void *q, pkv_dtype q_dtype,
 pkv_status pkv_testing_multiquery_attn_stall(const void *q, pkv_dtype q_dtype,
                                              const int32_t *cu_q, int32_t max_q_len,
                                              const void *k_cache, const void *v_cache,
+                                             const float *k_scales, const float *v_scales,
                                              const pkv_cache_desc *cache,
                                              const int32_t *block_tables,
                                              int32_t max_blocks_per_seq,

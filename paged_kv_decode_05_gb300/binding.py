@@ -56,9 +56,9 @@ _SIGS = {
                                        _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _DESC, _P, _P, _I32, _P, _P]),
     "pkv_multiquery_workspace_size": (_SZ, [_I32, _I32, _I32, _DESC, _I32]),
-    "pkv_multiquery_attn": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _DESC, _P, _I32,
-                                           _P, _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32,
-                                           _P, _P]),
+    "pkv_multiquery_attn": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _P, _P, _DESC, _P,
+                                           _I32, _P, _I32, _I32, ctypes.c_float, _P, _P, _SZ,
+                                           _I32, _P, _P]),
     "pkv_decode_attn_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32,
                                                _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P]),
     "pkv_merge_states": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P, _I32, _I32, _I32,
@@ -68,10 +68,10 @@ _SIGS = {
                                                      _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
                                                      _SZ, _I32, ctypes.c_uint64, _I32,
                                                      _P, _P]),
-    "pkv_testing_multiquery_attn_stall": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _DESC,
-                                                         _P, _I32, _P, _I32, _I32, ctypes.c_float,
-                                                         _P, _P, _SZ, _I32, ctypes.c_uint64,
-                                                         _I32, _P, _P]),
+    "pkv_testing_multiquery_attn_stall": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _P,
+                                                         _P, _DESC, _P, _I32, _P, _I32, _I32,
+                                                         ctypes.c_float, _P, _P, _SZ, _I32,
+                                                         ctypes.c_uint64, _I32, _P, _P]),
 }
 
 
@@ -232,12 +232,14 @@ def pkv_multiquery_workspace_size(batch, num_q_heads, max_q_len, k_cache, num_pa
 
 
 def pkv_multiquery_attn(q, cu_q, max_q_len, k_cache, v_cache, block_tables, context_lens,
-                        softmax_scale, out, workspace, num_parts=0, dev_status=None, stream=None):
-    """Causal attention of ``cu_q``-delimited new queries ``q [total_q, Hq, D]``."""
+                        softmax_scale, out, workspace, num_parts=0, dev_status=None, stream=None,
+                        k_scales=None, v_scales=None):
+    """Causal attention of ``cu_q``-delimited new queries ``q [total_q, Hq, D]``
+    (``k_scales``, ``v_scales``: INT8 caches only)."""
     desc = cache_desc(k_cache)
     code = lib().pkv_multiquery_attn(
         _ptr(q), _dtype_code(q), _ptr(cu_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
-        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
         int(cu_q.numel() - 1), int(q.shape[1]), float(softmax_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), int(num_parts), _ptr(dev_status),
         _stream(stream))
@@ -293,12 +295,13 @@ def pkv_testing_decode_attn_stall(q, k_cache, v_cache, block_tables, context_len
 
 def pkv_testing_multiquery_attn_stall(q, cu_q, max_q_len, k_cache, v_cache, block_tables,
                                       context_lens, softmax_scale, out, workspace, wait_limit_ns,
-                                      stall_cta, num_parts=0, dev_status=None, stream=None):
+                                      stall_cta, num_parts=0, dev_status=None, stream=None,
+                                      k_scales=None, v_scales=None):
     """Test hook: :func:`pkv_multiquery_attn` whose CTA ``stall_cta`` stalls."""
     desc = cache_desc(k_cache)
     code = lib().pkv_testing_multiquery_attn_stall(
         _ptr(q), _dtype_code(q), _ptr(cu_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
-        ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
         int(cu_q.numel() - 1), int(q.shape[1]), float(softmax_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), int(num_parts), int(wait_limit_ns),
         int(stall_cta), _ptr(dev_status), _stream(stream))

@@ -1,475 +1,14 @@
-// Multi-query paged attention: n_b new query tokens per sequence, causal
-// among themselves, over the paged KV cache (which already holds them).
-//
-// The target model of speculative decoding scores the draft's K tokens plus
-// one in a single batched pass (Continuous-Batching-LLM-Inference-Engine
-// README, feature list "Speculative decoding"); a continuous-batching
-// scheduler mixes decode tokens with prefill chunks (mini-inference-engine
-// overview, "decode tokens and prefill chunks"). Query i of sequence b sits at
-// position L_b - n_b + i and attends to positions 0 .. L_b - n_b + i.
-//
-// GB300 design. With n_b queries the g query heads of a KV head form
-// n_b * g rows that share every K/V tile: a real dense contraction, so the
-// math runs on the tensor cores (mma.sync m16n8k16, bf16/fp16 in, fp32
-// accumulate), FlashAttention-2 style:
-// * a CTA = NW consumer warps (16 rows each; a row tile of RT = 16 NW rows)
-//   + 1 producer warp. Work units are (sequence, kv head, row tile, block)
-//   with the blocks the tile's rows can see; the unit stream is cut into
-//   equal ranges per CTA (as in the decode kernel).
-// * The producer issues 2-D TMA tensor copies (cp.async.bulk.tensor) of each
-//   16-token K and V tile in 64-column boxes with the 128-byte swizzle into a
-//   ring of stages (full/empty mbarriers); consumers read B fragments with
-//   ldmatrix (K) and ldmatrix.trans (V) without bank conflicts.
-// * S = Q K^T (Q A fragments in registers), causal/length mask, online
-//   softmax in base 2 per row, P re-packed in registers as the A operand of
-//   O += P V. Rows of a piece that crosses ranges leave (m, l, o) partials;
-//   a combine kernel merges them.
+// Multi-query paged attention: the tcgen05 kernel for long query runs and
+// the host side of pkv_multiquery_attn (the mma.sync split kernel and its
+// combine live in mq_split.cuh).
 #include <cuda.h>
 
 #include <mutex>
 
-#include "common.cuh"
+#include "mq_split.cuh"
 
 namespace pkv {
 namespace {
-
-constexpr uint64_t kMqWaitNs = 4000000000ull;
-constexpr int kMqMaxBatch = 4096;
-constexpr float kMqLog2e = 1.4426950408889634f;
-
-struct MqParams {
-    const void* q;               // [total_q, hq, D]
-    const int32_t* cu_q;         // [B + 1]
-    const int32_t* block_tables; // [B, mb]
-    const int32_t* context_lens; // [B]
-    void* out;                   // [total_q, hq, D]
-    float* part_o;               // [slots, RT, D]
-    float* part_ml;              // [slots, RT, 2]
-    int32_t* ws_prefix;          // [B + 1] units before each sequence
-    uint32_t* status;
-    int batch, hq, hkv, mb, num_blocks, workers, tmax, max_q;
-    float qscale;                // softmax_scale * log2(e)
-    uint64_t wait_ns;            // limit of each bounded wait
-    int stall_cta;               // test hook: this CTA's first unit (split kernel) or
-                                 // first chunk (tcgen05 kernel) expects 16 bytes no
-                                 // copy delivers, so its wait runs out (-1: none)
-};
-
-// Blocks the rows of row tile t can see: its last query sits at position
-// L - n + min(n - 1, ((t + 1) RT - 1) / G).
-__host__ __device__ __forceinline__ int tile_blocks(int n, int L, int t, int RT, int G) {
-    const int q_last = min(n - 1, ((t + 1) * RT - 1) / G);
-    return (L - n + q_last) / kBlockSize + 1;
-}
-
-// Queries and length of sequence b, checked: max_q >= n >= 0, L >= n and L
-// within the table; an inconsistent sequence is treated as empty (flagged).
-__device__ __forceinline__ void seq_shape_raw(const int32_t* cu_q, const int32_t* lens, int b,
-                                              int mb, int max_q, int& n, int& L, bool& bad) {
-    n = cu_q[b + 1] - cu_q[b];
-    L = lens[b];
-    bad = n < 0 || n > max_q || L < n || L > mb * kBlockSize;
-    if (bad) n = L = 0;
-}
-__device__ __forceinline__ void seq_shape(const MqParams& p, int b, int& n, int& L, bool flag) {
-    bool bad;
-    seq_shape_raw(p.cu_q, p.context_lens, b, p.mb, p.max_q, n, L, bad);
-    if (bad && flag) flag_status(p.status, PKV_DEV_BAD_LENGTH);
-}
-
-// Units of one kv head of sequence b: sum over its row tiles of tile_blocks.
-__device__ __forceinline__ int seq_units_per_head(int n, int L, int RT, int G) {
-    if (n == 0) return 0;
-    const int T = (n * G + RT - 1) / RT;
-    int s = 0;
-    for (int t = 0; t < T; ++t) s += tile_blocks(n, L, t, RT, G);
-    return s;
-}
-
-// prefix[b] = units (all kv heads) before sequence b; all threads of the CTA.
-template <int NT>
-__device__ void mq_build_prefix(const MqParams& p, int* warp_tot, int* prefix, int RT, int G) {
-    const int t = threadIdx.x;
-    const int chunk = (p.batch + NT - 1) / NT;
-    const int lo = min(p.batch, t * chunk), hi = min(p.batch, lo + chunk);
-    const bool flag = blockIdx.x == 0;
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) {
-        int n, L;
-        seq_shape(p, i, n, L, flag);
-        sum += p.hkv * seq_units_per_head(n, L, RT, G);
-    }
-    const int lane = t & 31, warp = t >> 5;
-    int inc = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFull, inc, o);
-        if (lane >= o) inc += v;
-    }
-    if (lane == 31) warp_tot[warp] = inc;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += warp_tot[w];
-    int run = base + inc - sum;
-    for (int i = lo; i < hi; ++i) {
-        prefix[i] = run;
-        int n, L;
-        seq_shape(p, i, n, L, false);
-        run += p.hkv * seq_units_per_head(n, L, RT, G);
-    }
-    if (t == NT - 1) prefix[p.batch] = run;
-    __syncthreads();
-    if (blockIdx.x == 0)
-        for (int i = t; i <= p.batch; i += NT) p.ws_prefix[i] = prefix[i];
-}
-
-// Unit u -> (b, kv head, row tile t, block j, n, L).
-__device__ __forceinline__ void mq_decode_unit(const MqParams& p, const int* prefix, int u, int RT,
-                                               int G, int& b, int& kvh, int& t, int& j, int& n,
-                                               int& L) {
-    int lo = 0;
-    for (int step = 1 << 12; step; step >>= 1)  // kMqMaxBatch = 2^12
-        if (lo + step < p.batch && prefix[lo + step] <= u) lo += step;
-    b = lo;
-    seq_shape(p, b, n, L, false);
-    const int per_head = seq_units_per_head(n, L, RT, G);
-    int r = u - prefix[b];
-    kvh = r / per_head;
-    r -= kvh * per_head;
-    t = 0;
-    for (;;) {
-        const int nb = tile_blocks(n, L, t, RT, G);
-        if (r < nb) break;
-        r -= nb;
-        ++t;
-    }
-    j = r;
-}
-
-// ------------------------------------------------------------ PTX helpers ---
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                              uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-// 2-D tiled TMA load of box (x, y) of `tmap` into shared memory at `dst`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tmap, int x, int y,
-                                            uint32_t bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3}], [%4];"
-                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
-                 : "memory");
-}
-
-// Byte offset of (row r, 16-byte chunk c) inside one 16 x 128-byte sub-tile
-// written by TMA with the 128-byte swizzle (chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-template <int D, int NW>
-struct MqCfg {
-    // ring depth (6 stages measured slower than 4 for the 32-row variant)
-    static constexpr int NS = 4;
-    static constexpr int RT = 16 * NW;                 // rows per tile
-    static constexpr int NT = 32 * (NW + 1);           // threads: NW consumers + producer
-    static constexpr int SUB = 16 * 128;               // one 16 x 64-element sub-tile
-    static constexpr int NSUB = D / 64;                // sub-tiles per K (or V) tile
-    static constexpr int TILE = NSUB * SUB;
-    static constexpr int STAGE = 2 * TILE;             // K then V
-    static constexpr int OFF_FULL = NS * STAGE;
-    static constexpr int OFF_EMPTY = OFF_FULL + NS * 8;
-    static constexpr int OFF_META = OFF_EMPTY + NS * 8;   // 2 x int4 per stage
-    static constexpr int OFF_SCAN = OFF_META + NS * 32;
-    static constexpr int OFF_PREFIX = OFF_SCAN + 32;
-    // dynamic shared memory: alignment slack + the layout above + the prefix
-    static constexpr int fixed_bytes() { return 1024 + OFF_PREFIX; }
-    static_assert(D == 64 || D == 128, "head_dim");
-};
-
-__device__ __forceinline__ long long mq_eff_workers(long long U, long long W) {
-    const long long cap = U / 4;   // at least 4 units per range: ranges are never empty
-    return cap < 1 ? 1 : (cap < W ? cap : W);
-}
-
-template <typename KV, int D, int G, int NW>
-__global__ void __launch_bounds__(32 * (NW + 1))
-mq_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                const MqParams p) {
-    using C = MqCfg<D, NW>;
-    constexpr int NS = C::NS;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_FULL);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + C::OFF_EMPTY);
-    int4* meta = reinterpret_cast<int4*>(smem + C::OFF_META);
-    int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    griddep_wait();
-    griddep_launch_dependents();
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), NW);
-        }
-        fence_mbar_init();
-    }
-    mq_build_prefix<C::NT>(p, reinterpret_cast<int*>(smem + C::OFF_SCAN), prefix, C::RT, G);
-    const long long U = prefix[p.batch];
-    const long long W = mq_eff_workers(U, p.workers);
-    const long long wk = blockIdx.x;
-    if (wk >= W || U == 0) return;
-    const int u0 = int(wk * U / W), u1 = int((wk + 1) * U / W);
-
-    if (warp == NW) {
-        // ------------------------------------------------------ producer ---
-        auto fetch = [&](int base, int& b, int& kvh, int& t, int& j, int& n, int& L, int& blk,
-                         int& cu) {
-            const int u = base + lane;
-            if (u < u1) {
-                mq_decode_unit(p, prefix, u, C::RT, G, b, kvh, t, j, n, L);
-                blk = __ldg(p.block_tables + (long long)b * p.mb + j);
-                cu = __ldg(p.cu_q + b);
-            } else {
-                b = kvh = t = j = n = L = cu = 0;
-                blk = -1;
-            }
-        };
-        int cbase = u0;
-        int cb, ck, ct, cj, cn, cL, cblk, ccu, xb, xk, xt, xj, xn, xL, xblk, xcu;
-        fetch(cbase, cb, ck, ct, cj, cn, cL, cblk, ccu);
-        fetch(cbase + 32, xb, xk, xt, xj, xn, xL, xblk, xcu);
-        uint32_t parity = 0;
-        int s = 0;
-        for (int u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1) {
-            int idx = u - cbase;
-            if (idx >= 32) {
-                cbase += 32;
-                cb = xb; ck = xk; ct = xt; cj = xj; cn = xn; cL = xL; cblk = xblk; ccu = xcu;
-                fetch(cbase + 32, xb, xk, xt, xj, xn, xL, xblk, xcu);
-                idx -= 32;
-            }
-            const int b = __shfl_sync(kFull, cb, idx), kvh = __shfl_sync(kFull, ck, idx);
-            const int t = __shfl_sync(kFull, ct, idx), j = __shfl_sync(kFull, cj, idx);
-            const int n = __shfl_sync(kFull, cn, idx), L = __shfl_sync(kFull, cL, idx);
-            const int blk = __shfl_sync(kFull, cblk, idx), cu = __shfl_sync(kFull, ccu, idx);
-            if (u - u0 >= NS) {  // wait until every consumer released this stage
-                const bool ok = mbar_wait_bounded(smem_addr(&empty[s]), (parity >> s) & 1u, p.wait_ns);
-                parity ^= 1u << s;
-                if (!__all_sync(kFull, ok)) {   // records where it gave up: bit 9
-                    if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT | 0x200u);
-                    return;
-                }
-            }
-            if (lane == 0) {
-                const uint32_t bar = smem_addr(&full[s]);
-                const bool valid = unsigned(blk) < unsigned(p.num_blocks);
-                const uint32_t extra = (u == u0 && wk == p.stall_cta) ? 16u : 0u;
-                meta[2 * s] = make_int4(b, kvh, t, j);
-                // (n, L, cu_q[b], flags: bit 0 = block valid, bit 1 = first unit of a piece)
-                meta[2 * s + 1] = make_int4(n, L, cu, (valid ? 1 : 0) | ((u == u0 || j == 0) ? 2 : 0));
-                if (valid) {
-                    const int y = (blk * p.hkv + kvh) * kBlockSize;
-                    unsigned char* st = smem + s * C::STAGE;
-                    mbar_arrive_expect_tx(bar, C::STAGE + extra);
-#pragma unroll
-                    for (int sub = 0; sub < C::NSUB; ++sub) {
-                        tma_load_2d(smem_addr(st + sub * C::SUB), &tmk, 64 * sub, y, bar);
-                        tma_load_2d(smem_addr(st + C::TILE + sub * C::SUB), &tmv, 64 * sub, y, bar);
-                    }
-                } else {
-                    flag_status(p.status, PKV_DEV_BAD_BLOCK);
-                    if (extra) mbar_arrive_expect_tx(bar, extra);
-                    else mbar_arrive(bar);
-                }
-            }
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------- consumers ---
-    const int gq = lane >> 2, tq = lane & 3;
-    uint32_t qa[D / 16][4];          // Q A fragments of the warp's 16 rows
-    float o[D / 8][4];               // O accumulators: rows gq (0,1), gq + 8 (2,3)
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    int pb = -1, pk = 0, pt = 0, pn = 0, pL = 0, first_j = 0, last_j = 0;
-    bool v0 = false, v1 = false;     // rows gq / gq + 8 exist (per lane)
-    bool wact = false;               // the warp covers at least one row (warp-uniform)
-    int pos0 = 0, pos1 = 0;          // their query positions
-    long long orow0 = 0, orow1 = 0;  // their q / out element offsets
-
-    auto finalize = [&]() {
-        float a = l0, c = l1;
-        a += __shfl_xor_sync(kFull, a, 1); a += __shfl_xor_sync(kFull, a, 2);
-        c += __shfl_xor_sync(kFull, c, 1); c += __shfl_xor_sync(kFull, c, 2);
-        if (!v0 && !v1) return;
-        const bool whole = first_j == 0 && last_j == tile_blocks(pn, pL, pt, C::RT, G) - 1;
-        if (whole) {
-            const float i0 = a > 0.f ? 1.f / a : 0.f, i1 = c > 0.f ? 1.f / c : 0.f;
-            uint32_t* out = static_cast<uint32_t*>(p.out);
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                if (v0) out[(orow0 + 8 * nd + 2 * tq) / 2] = pack2<KV>(o[nd][0] * i0, o[nd][1] * i0);
-                if (v1) out[(orow1 + 8 * nd + 2 * tq) / 2] = pack2<KV>(o[nd][2] * i1, o[nd][3] * i1);
-            }
-        } else {
-            const long long slot = ((long long)pb * p.hkv + pk) * p.tmax + pt + wk;
-            const long long r0 = slot * C::RT + warp * 16 + gq, r1 = r0 + 8;
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                if (v0) *reinterpret_cast<float2*>(p.part_o + r0 * D + 8 * nd + 2 * tq) =
-                            make_float2(o[nd][0], o[nd][1]);
-                if (v1) *reinterpret_cast<float2*>(p.part_o + r1 * D + 8 * nd + 2 * tq) =
-                            make_float2(o[nd][2], o[nd][3]);
-            }
-            if (tq == 0) {
-                if (v0) *reinterpret_cast<float2*>(p.part_ml + r0 * 2) = make_float2(m0, a);
-                if (v1) *reinterpret_cast<float2*>(p.part_ml + r1 * 2) = make_float2(m1, c);
-            }
-        }
-    };
-
-    uint32_t parity = 0;
-    int s = 0;
-    bool aborted = false;
-    for (int u = u0; u < u1; ++u, s = (s + 1 == NS) ? 0 : s + 1) {
-        const bool got = mbar_wait_bounded(smem_addr(&full[s]), (parity >> s) & 1u, p.wait_ns);
-        parity ^= 1u << s;
-        if (!__all_sync(kFull, got)) {          // records where it gave up: bit 8
-            if (lane == 0) flag_status(p.status, PKV_DEV_TIMEOUT | 0x100u);
-            aborted = true;
-            break;
-        }
-        const int4 ma = meta[2 * s], mb = meta[2 * s + 1];
-        if (mb.w & 2) {  // first unit of a new piece: load the warp's Q rows
-            if (pb >= 0) finalize();
-            pb = ma.x; pk = ma.y; pt = ma.z; first_j = ma.w; pn = mb.x; pL = mb.y;
-            const int rr0 = pt * C::RT + warp * 16 + gq, rr1 = rr0 + 8;
-            v0 = rr0 < pn * G;
-            v1 = rr1 < pn * G;
-            // warp-uniform: the collective ldmatrix / mma / shuffles below
-            // must be reached by all 32 lanes or by none
-            wact = pt * C::RT + warp * 16 < pn * G;
-            const int cu = mb.z;
-            orow0 = ((long long)(cu + rr0 / G) * p.hq + pk * G + rr0 % G) * D;
-            orow1 = ((long long)(cu + rr1 / G) * p.hq + pk * G + rr1 % G) * D;
-            pos0 = pL - pn + rr0 / G;
-            pos1 = pL - pn + rr1 / G;
-            const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                qa[kk][0] = v0 ? __ldg(q32 + (orow0 + 16 * kk + 2 * tq) / 2) : 0u;
-                qa[kk][1] = v1 ? __ldg(q32 + (orow1 + 16 * kk + 2 * tq) / 2) : 0u;
-                qa[kk][2] = v0 ? __ldg(q32 + (orow0 + 16 * kk + 2 * tq + 8) / 2) : 0u;
-                qa[kk][3] = v1 ? __ldg(q32 + (orow1 + 16 * kk + 2 * tq + 8) / 2) : 0u;
-            }
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-        }
-        last_j = ma.w;
-        bool zeroed = false;
-        if ((mb.w & 1) && wact) {
-            unsigned char* kt = smem + s * C::STAGE;
-            unsigned char* vt = kt + C::TILE;
-            const int j = ma.w;
-            const int nvt = min(kBlockSize, pL - kBlockSize * j);   // tokens present in the tile
-            if (nvt < kBlockSize) {  // stale rows may hold NaN: P.V must read zeros there
-                for (int off = lane * 16; off < (kBlockSize - nvt) * 128; off += 32 * 16)
-#pragma unroll
-                    for (int sub = 0; sub < C::NSUB; ++sub)
-                        *reinterpret_cast<uint4*>(vt + sub * C::SUB + nvt * 128 + off) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                zeroed = true;
-                __syncwarp();
-            }
-            // S = Q K^T for the 16 tokens of the tile (two n8 tiles)
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const int mi = lane >> 3, r8 = lane & 7;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int tok = ((mi & 2) ? 8 : 0) + r8, c = 2 * (kk % 4) + (mi & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(smem_addr(kt + (kk / 4) * C::SUB) + swz(tok, c), b0, b1, b2, b3);
-                mma16816<KV>(sc[0], qa[kk], b0, b1);
-                mma16816<KV>(sc[1], qa[kk], b2, b3);
-            }
-            // causal + length mask, online softmax per row (base 2)
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = kBlockSize * j + 8 * nn + 2 * tq + e;
-                    sc[nn][e] = (v0 && col <= pos0) ? sc[nn][e] * p.qscale : -INFINITY;
-                    sc[nn][2 + e] = (v1 && col <= pos1) ? sc[nn][2 + e] * p.qscale : -INFINITY;
-                    mx0 = fmaxf(mx0, sc[nn][e]);
-                    mx1 = fmaxf(mx1, sc[nn][2 + e]);
-                }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
-            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
-            const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
-            m0 = n0;
-            m1 = n1;
-            float pr[2][4];
-#pragma unroll
-            for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float mr = e < 2 ? n0 : n1;
-                    pr[nn][e] = (sc[nn][e] == -INFINITY) ? 0.f : fast_exp2(sc[nn][e] - mr);
-                }
-            l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-            l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-            // P = hi + lo in two 16-bit parts (lo = rn(P - hi), the difference
-            // exact in fp32): a row that sees two or three tokens would
-            // otherwise carry the 2^-9 rounding of a bf16 weight into its output
-            uint32_t pa[4], pl[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float x = pr[k >> 1][2 * (k & 1)], y = pr[k >> 1][2 * (k & 1) + 1];
-                pa[k] = pack2<KV>(x, y);
-                const float2 r = unpack2(KV{}, pa[k]);
-                pl[k] = pack2<KV>(x - r.x, y - r.y);
-            }
-            // O = O * alpha + P V (the rescale only when some running max moved;
-            // the vote is warp-uniform)
-            if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
-#pragma unroll
-                for (int nd = 0; nd < D / 8; ++nd) {
-                    o[nd][0] *= a0; o[nd][1] *= a0; o[nd][2] *= a1; o[nd][3] *= a1;
-                }
-            }
-#pragma unroll
-            for (int ndp = 0; ndp < D / 16; ++ndp) {
-                const int tok = ((mi & 1) ? 8 : 0) + r8, c = 2 * (ndp % 4) + (mi >> 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(smem_addr(vt + (ndp / 4) * C::SUB) + swz(tok, c), b0, b1, b2, b3);
-                mma16816<KV>(o[2 * ndp], pa, b0, b1);
-                mma16816<KV>(o[2 * ndp + 1], pa, b2, b3);
-                mma16816<KV>(o[2 * ndp], pl, b0, b1);
-                mma16816<KV>(o[2 * ndp + 1], pl, b2, b3);
-            }
-        }
-        // release the stage; generic-proxy writes (the zeroing) must be
-        // ordered before the next asynchronous (TMA) write into it
-        if (zeroed) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-    }
-    if (!aborted && pb >= 0) finalize();
-}
 
 // ------------------------------------------------- tcgen05 row-tile kernel ---
 // Long query runs (prefill chunks): a CTA owns two tiles of 128 rows of one
@@ -933,75 +472,6 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::TMEM_COLS));
 }
 
-// ---------------------------------------------------------------- combine ---
-struct MqCombine {
-    const float* part_o;
-    const float* part_ml;
-    const int32_t* ws_prefix;
-    const int32_t* cu_q;
-    const int32_t* context_lens;
-    void* out;
-    int batch, hq, hkv, mb, workers, tmax, max_q;
-};
-
-__device__ __forceinline__ void mq_merge(float& M, float& den, float4& num, float m, float l,
-                                         const float4& o) {
-    if (m == -INFINITY) return;
-    if (m > M) {
-        const float r = (M == -INFINITY) ? 0.f : fast_exp2(M - m);
-        den *= r;
-        num.x *= r; num.y *= r; num.z *= r; num.w *= r;
-        M = m;
-    }
-    const float a = fast_exp2(m - M);
-    den += a * l;
-    num.x += a * o.x; num.y += a * o.y; num.z += a * o.z; num.w += a * o.w;
-}
-
-// One CTA per (sequence, kv head, row tile): merge the pieces of every row
-// (skipping tiles finished inside one range and tiles that do not exist).
-template <typename KV, int D, int G, int RT>
-__global__ void __launch_bounds__(256) mq_combine_kernel(const MqCombine c) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const long long sidx = blockIdx.x;
-    const int b = int(sidx / ((long long)c.hkv * c.tmax));
-    const int rem = int(sidx - (long long)b * c.hkv * c.tmax);
-    const int kvh = rem / c.tmax, t = rem - kvh * c.tmax;
-    int n, L;
-    bool bad;
-    seq_shape_raw(c.cu_q, c.context_lens, b, c.mb, c.max_q, n, L, bad);
-    if (n == 0 || t * RT >= n * G) return;
-    const int per_head = seq_units_per_head(n, L, RT, G);
-    int cum = 0;
-    for (int tt = 0; tt < t; ++tt) cum += tile_blocks(n, L, tt, RT, G);
-    const long long U = c.ws_prefix[c.batch];
-    const long long W = mq_eff_workers(U, c.workers);
-    const long long uf = (long long)c.ws_prefix[b] + (long long)kvh * per_head + cum;
-    const long long ul = uf + tile_blocks(n, L, t, RT, G) - 1;
-    const long long wf = ((uf + 1) * W - 1) / U, wl = ((ul + 1) * W - 1) / U;
-    if (wf == wl) return;
-    const int rows = min(RT, n * G - t * RT);
-    const int cu = c.cu_q[b];
-    for (int it = threadIdx.x; it < rows * (D / 4); it += blockDim.x) {
-        const int row = it / (D / 4), d4 = it - row * (D / 4);
-        float M = -INFINITY, den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (long long w = wf; w <= wl; ++w) {
-            const long long r = (sidx + w) * RT + row;
-            const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + r * 2);
-            const float4 o = *reinterpret_cast<const float4*>(c.part_o + r * D + 4 * d4);
-            mq_merge(M, den, num, ml.x, ml.y, o);
-        }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const int rr = t * RT + row;
-        const long long e = ((long long)(cu + rr / G) * c.hq + kvh * G + rr % G) * D + 4 * d4;
-        uint32_t* out = static_cast<uint32_t*>(c.out);
-        out[e / 2] = pack2<KV>(num.x * inv, num.y * inv);
-        out[e / 2 + 1] = pack2<KV>(num.z * inv, num.w * inv);
-    }
-}
-
 // ------------------------------------------------------------------- host ---
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1037,65 +507,6 @@ bool encode_cache_map(CUtensorMap* m, const void* base, bool bf16, int D, long l
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct MqOps {
-    int fixed_smem, rt, threads;
-    cudaError_t (*prepare)(size_t smem);
-    cudaError_t (*occupancy)(int* blocks, size_t smem);
-    cudaError_t (*split)(const CUtensorMap&, const CUtensorMap&, const MqParams&, int, size_t,
-                         cudaStream_t);
-    cudaError_t (*combine)(const MqCombine&, int, cudaStream_t);
-};
-
-template <typename KV, int D, int G, int NW>
-struct MqImpl {
-    using C = MqCfg<D, NW>;
-    static cudaError_t prepare(size_t smem) {
-        return cudaFuncSetAttribute(mq_split_kernel<KV, D, G, NW>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    }
-    static cudaError_t occupancy(int* blocks, size_t smem) {
-        cudaError_t e = prepare(smem);
-        if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mq_split_kernel<KV, D, G, NW>,
-                                                             C::NT, smem);
-    }
-    static cudaError_t split(const CUtensorMap& k, const CUtensorMap& v, const MqParams& p,
-                             int grid, size_t smem, cudaStream_t st) {
-        return launch_pdl(mq_split_kernel<KV, D, G, NW>, dim3(grid), dim3(C::NT), smem, st, k, v, p);
-    }
-    static cudaError_t combine(const MqCombine& c, int grid, cudaStream_t st) {
-        return launch_pdl(mq_combine_kernel<KV, D, G, C::RT>, dim3(grid), dim3(256), 0, st, c);
-    }
-    static MqOps ops() {
-        return MqOps{C::fixed_bytes(), C::RT, C::NT, prepare, occupancy, split, combine};
-    }
-};
-
-template <typename KV, int D, int G>
-bool mq_pick_nw(int nw, MqOps* o) {
-    switch (nw) {
-        case 1: *o = MqImpl<KV, D, G, 1>::ops(); return true;
-        case 2: *o = MqImpl<KV, D, G, 2>::ops(); return true;
-        case 4: *o = MqImpl<KV, D, G, 4>::ops(); return true;
-    }
-    return false;
-}
-template <typename KV, int D>
-bool mq_pick_g(int G, int nw, MqOps* o) {
-    switch (G) {
-        case 1: return mq_pick_nw<KV, D, 1>(nw, o);
-        case 2: return mq_pick_nw<KV, D, 2>(nw, o);
-        case 4: return mq_pick_nw<KV, D, 4>(nw, o);
-    }
-    return false;
-}
-template <typename KV>
-bool mq_pick_d(int D, int G, int nw, MqOps* o) {
-    if (D == 128) return mq_pick_g<KV, 128>(G, nw, o);
-    if (D == 64) return mq_pick_g<KV, 64>(G, nw, o);
-    return false;
-}
-
 // tcgen05 row-tile path: launchers by cache type, head dim and group size.
 using TcLaunch = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const MqParams&, int,
                                  cudaStream_t);
@@ -1117,6 +528,7 @@ TcLaunch tc_pick_g(int G) {
         case 1: return tc_launch<KV, D, 1>;
         case 2: return tc_launch<KV, D, 2>;
         case 4: return tc_launch<KV, D, 4>;
+        case 8: return tc_launch<KV, D, 8>;
     }
     return nullptr;
 }
@@ -1144,8 +556,10 @@ pkv_status mq_plan(const pkv_cache_desc* c, int batch, int hq, int max_q, pkv_dt
         return PKV_ERR_INVALID_ARG;
     if (batch < 0 || hq <= 0 || hq % c->num_kv_heads || max_q <= 0 || num_parts < 0)
         return PKV_ERR_INVALID_ARG;
-    if (c->kv_dtype != PKV_BF16 && c->kv_dtype != PKV_F16) return PKV_ERR_UNSUPPORTED;
-    if (q_dtype != c->kv_dtype) return PKV_ERR_INVALID_ARG;
+    if (c->kv_dtype != PKV_BF16 && c->kv_dtype != PKV_F16 && c->kv_dtype != PKV_I8)
+        return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_BF16 && q_dtype != PKV_F16) return PKV_ERR_INVALID_ARG;
+    if (c->kv_dtype != PKV_I8 && q_dtype != c->kv_dtype) return PKV_ERR_INVALID_ARG;
     if (c->block_size != kBlockSize || batch > kMqMaxBatch) return PKV_ERR_UNSUPPORTED;
     if ((long long)c->num_blocks * c->num_kv_heads * kBlockSize >= (1LL << 31))
         return PKV_ERR_UNSUPPORTED;
@@ -1153,8 +567,12 @@ pkv_status mq_plan(const pkv_cache_desc* c, int batch, int hq, int max_q, pkv_dt
     const long long rows = (long long)max_q * pl->G;
     if (rows > (1LL << 24)) return PKV_ERR_UNSUPPORTED;
     pl->nw = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
-    const bool ok = c->kv_dtype == PKV_BF16 ? mq_pick_d<BF16>(c->head_dim, pl->G, pl->nw, &pl->ops)
-                                            : mq_pick_d<F16>(c->head_dim, pl->G, pl->nw, &pl->ops);
+    bool ok;
+    if (c->kv_dtype == PKV_I8)
+        ok = mq_pick_i8(q_dtype, c->head_dim, pl->G, pl->nw, &pl->ops);
+    else
+        ok = c->kv_dtype == PKV_BF16 ? mq_pick_d<BF16, BF16>(c->head_dim, pl->G, pl->nw, &pl->ops)
+                                     : mq_pick_d<F16, F16>(c->head_dim, pl->G, pl->nw, &pl->ops);
     if (!ok) return PKV_ERR_UNSUPPORTED;
     pl->tmax = int((rows + pl->ops.rt - 1) / pl->ops.rt);
     pl->smem = size_t(pl->ops.fixed_smem) + 4 * size_t((batch < 1 ? 1 : batch) + 1);
@@ -1186,8 +604,8 @@ extern "C" size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_hea
                                                 int32_t num_parts) {
     MqPlan pl;
     if (!cache) return 0;
-    if (mq_plan(cache, batch, num_q_heads, max_q_len, cache->kv_dtype, num_parts, &pl) != PKV_OK)
-        return 0;
+    const pkv_dtype qd = cache->kv_dtype == PKV_I8 ? PKV_BF16 : cache->kv_dtype;   // same sizes
+    if (mq_plan(cache, batch, num_q_heads, max_q_len, qd, num_parts, &pl) != PKV_OK) return 0;
     return pl.ws_total;
 }
 
@@ -1197,6 +615,7 @@ constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
                           int32_t max_q_len, const void* k_cache, const void* v_cache,
+                          const float* k_scales, const float* v_scales,
                           const pkv_cache_desc* cache, const int32_t* block_tables,
                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
                           int32_t num_q_heads, float softmax_scale, void* out, void* workspace,
@@ -1215,16 +634,21 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     if (max_blocks_per_seq <= 0 || !(softmax_scale == softmax_scale) || softmax_scale > 3.0e38f ||
         softmax_scale < -3.0e38f || pl.workers > 0x7fffffffLL)
         return PKV_ERR_INVALID_ARG;
+    const bool i8 = cache->kv_dtype == PKV_I8;
+    if (i8 && (!k_scales || !v_scales || !mq_aligned(k_scales, 4) || !mq_aligned(v_scales, 4) ||
+               !mq_aligned(q, 16)))
+        return PKV_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < pl.ws_total || !mq_aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     const long long rows = (long long)cache->num_blocks * cache->num_kv_heads * kBlockSize;
-    CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows) ||
-        !encode_cache_map(&tv, v_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows))
+    CUtensorMap tk = {}, tv = {};   // INT8 tiles are read by 1-D bulk copies instead
+    if (!i8 && (!encode_cache_map(&tk, k_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows) ||
+                !encode_cache_map(&tv, v_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows)))
         return PKV_ERR_CUDA;
-    // Query runs that fill 128-row tiles take the tcgen05 kernel (no split,
-    // no combine, no workspace); shorter ones the mma.sync kernel below.
-    const TcLaunch tc = ((long long)max_q_len * pl.G >= kTcRows && mq_aligned(q, 16) &&
+    // Query runs of 16-bit caches that fill 128-row tiles take the tcgen05
+    // kernel (no split, no combine, no workspace); shorter runs, and every run
+    // over an INT8 cache, the mma.sync kernel below.
+    const TcLaunch tc = (!i8 && (long long)max_q_len * pl.G >= kTcRows && mq_aligned(q, 16) &&
                          mq_aligned(out, 16))
                             ? (cache->kv_dtype == PKV_BF16 ? tc_pick<BF16>(cache->head_dim, pl.G)
                                                            : tc_pick<F16>(cache->head_dim, pl.G))
@@ -1261,7 +685,10 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     p.wait_ns = wait_ns;
     p.stall_cta = stall_cta;
     if (pl.ops.prepare(pl.smem) != cudaSuccess) return PKV_ERR_CUDA;
-    if (pl.ops.split(tk, tv, p, int(pl.workers), pl.smem, stream) != cudaSuccess)
+    const MqI8Src ik{k_cache, k_scales}, iv{v_cache, v_scales};
+    const void* ks = i8 ? static_cast<const void*>(&ik) : static_cast<const void*>(&tk);
+    const void* vs = i8 ? static_cast<const void*>(&iv) : static_cast<const void*>(&tv);
+    if (pl.ops.split(ks, vs, p, int(pl.workers), pl.smem, stream) != cudaSuccess)
         return PKV_ERR_CUDA;
     MqCombine cb;
     cb.part_o = p.part_o; cb.part_ml = p.part_ml; cb.ws_prefix = p.ws_prefix; cb.cu_q = cu_q;
@@ -1278,17 +705,18 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
 
 extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
                                           int32_t max_q_len, const void* k_cache,
-                                          const void* v_cache, const pkv_cache_desc* cache,
+                                          const void* v_cache, const float* k_scales,
+                                          const float* v_scales, const pkv_cache_desc* cache,
                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
                                           const int32_t* context_lens, int32_t batch,
                                           int32_t num_q_heads, float softmax_scale, void* out,
                                           void* workspace, size_t workspace_bytes,
                                           int32_t num_parts, uint32_t* dev_status,
                                           cudaStream_t stream) {
-    return run_multiquery(q, q_dtype, cu_q, max_q_len, k_cache, v_cache, cache, block_tables,
-                          max_blocks_per_seq, context_lens, batch, num_q_heads, softmax_scale, out,
-                          workspace, workspace_bytes, num_parts, dev_status, stream, kMqWaitNs,
-                          -1);
+    return run_multiquery(q, q_dtype, cu_q, max_q_len, k_cache, v_cache, k_scales, v_scales,
+                          cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                          num_q_heads, softmax_scale, out, workspace, workspace_bytes, num_parts,
+                          dev_status, stream, kMqWaitNs, -1);
 }
 
 // ------------------------------------------------------------- test hook ---
@@ -1296,13 +724,14 @@ extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, cons
 
 extern "C" pkv_status pkv_testing_multiquery_attn_stall(
     const void* q, pkv_dtype q_dtype, const int32_t* cu_q, int32_t max_q_len, const void* k_cache,
-    const void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+    const void* v_cache, const float* k_scales, const float* v_scales,
+    const pkv_cache_desc* cache, const int32_t* block_tables,
     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
     float softmax_scale, void* out, void* workspace, size_t workspace_bytes, int32_t num_parts,
     uint64_t wait_limit_ns, int32_t stall_cta, uint32_t* dev_status, cudaStream_t stream) {
     if (wait_limit_ns > kMqWaitNs || stall_cta < -1) return PKV_ERR_INVALID_ARG;
-    return run_multiquery(q, q_dtype, cu_q, max_q_len, k_cache, v_cache, cache, block_tables,
-                          max_blocks_per_seq, context_lens, batch, num_q_heads, softmax_scale, out,
-                          workspace, workspace_bytes, num_parts, dev_status, stream, wait_limit_ns,
-                          stall_cta);
+    return run_multiquery(q, q_dtype, cu_q, max_q_len, k_cache, v_cache, k_scales, v_scales,
+                          cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                          num_q_heads, softmax_scale, out, workspace, workspace_bytes, num_parts,
+                          dev_status, stream, wait_limit_ns, stall_cta);
 }

@@ -112,6 +112,10 @@ CONFIGS = {
         name="prefill_chunk", batch=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
         kv_dtype="bf16", q_dtype="bf16", src_dtype="bf16",
         len_groups=((8, 512, 8192),), max_len=8192, q_len=512),
+    "spec_verify_int8": DecodeConfig(
+        name="spec_verify_int8", batch=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        kv_dtype="i8", q_dtype="bf16", src_dtype="bf16",
+        len_groups=((256, 128, 4096),), max_len=4096, q_len=5),
 }
 
 # One-line workload descriptions, for bench output and docs.
@@ -128,6 +132,8 @@ DESCRIPTIONS = {
                    "32/8 heads, D=128, L~U[128,4096]",
     "prefill_chunk": "chunked prefill bf16: B=8, 512-token chunk per sequence after a cached "
                      "prefix, 32/8 heads, D=128, L~U[512,8192]",
+    "spec_verify_int8": "speculative verification over an INT8 cache: B=256, 4 draft tokens + 1 "
+                        "per sequence, 32/8 heads, D=128, L~U[128,4096]",
 }
 
 

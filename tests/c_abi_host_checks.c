@@ -100,12 +100,15 @@ int main(void) {
                                   0, 32, 0.125f, fake, 64, NULL, NULL) == PKV_OK);   /* empty */
 
     /* multi-query attention and block copy */
-    CHECK(pkv_multiquery_attn(fake, PKV_BF16, fake, 5, fake, fake, &bf16, fake, 4, fake, 4, 64,
-                              0.125f, fake, fake, 1u << 30, 16, NULL, NULL) ==
-          PKV_ERR_UNSUPPORTED);                                     /* group 8 */
-    CHECK(pkv_multiquery_attn(fake, PKV_BF16, fake, 0, fake, fake, &bf16, fake, 4, fake, 4, 32,
-                              0.125f, fake, fake, 1u << 30, 16, NULL, NULL) ==
+    CHECK(pkv_multiquery_attn(fake, PKV_BF16, fake, 5, fake, fake, NULL, NULL, &bf16, fake, 4,
+                              fake, 4, 128, 0.125f, fake, fake, 1u << 30, 16, NULL, NULL) ==
+          PKV_ERR_UNSUPPORTED);                                     /* group 16 */
+    CHECK(pkv_multiquery_attn(fake, PKV_BF16, fake, 0, fake, fake, NULL, NULL, &bf16, fake, 4,
+                              fake, 4, 32, 0.125f, fake, fake, 1u << 30, 16, NULL, NULL) ==
           PKV_ERR_INVALID_ARG);                                     /* max_q_len 0 */
+    CHECK(pkv_multiquery_attn(fake, PKV_BF16, fake, 5, fake, fake, NULL, NULL, &i8, fake, 4,
+                              fake, 4, 32, 0.125f, fake, fake, 1u << 30, 16, NULL, NULL) ==
+          PKV_ERR_INVALID_ARG);                                     /* INT8 needs scales */
     CHECK(pkv_copy_blocks(fake, fake, NULL, NULL, &bf16, fake, fake, 0, NULL, NULL) == PKV_OK);
     CHECK(pkv_copy_blocks(fake, fake, NULL, NULL, &bf16, fake, fake, -1, NULL, NULL) ==
           PKV_ERR_INVALID_ARG);

@@ -123,14 +123,16 @@ def test_multiquery_and_copy_blocks_host_validation(lib):
 
     def mq(q_dtype=B.PKV_BF16, dd=None, batch=4, hq=8, max_q=5, ws=fake, ws_bytes=1 << 30,
            parts=16):
-        return lib.pkv_multiquery_attn(fake, q_dtype, fake, max_q, fake, fake,
+        return lib.pkv_multiquery_attn(fake, q_dtype, fake, max_q, fake, fake, scales, scales,
                                        ctypes.byref(dd or d), fake, 4, fake, batch, hq, 0.125,
                                        fake, ws, ws_bytes, parts, None, None)
+    scales = None
     assert mq(hq=7) == 1                         # heads not a multiple of kv heads
-    assert mq(hq=16) == 2                        # group 8 not built
+    assert mq(hq=32) == 2                        # group 16 not built
     assert mq(max_q=0) == 1
-    assert mq(q_dtype=B.PKV_F16) == 1            # q dtype must match the cache
-    assert mq(dd=desc(dt=B.PKV_I8)) == 2         # INT8 caches not supported here
+    assert mq(q_dtype=B.PKV_F16) == 1            # q dtype must match a 16-bit cache
+    assert mq(q_dtype=B.PKV_I8) == 1             # q is never INT8
+    assert mq(dd=desc(dt=B.PKV_I8)) == 1         # INT8 caches need their scales
     assert mq(dd=desc(d=96)) == 2
     assert mq(batch=5000) == 2
     assert mq(batch=0) == 0

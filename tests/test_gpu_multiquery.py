@@ -1,6 +1,7 @@
 """GPU parity: pkv_multiquery_attn (speculative verification, prefill chunks)
 against the float64 causal oracle. Tolerance as for decode:
-|gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise."""
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise for fp16 / bf16 caches,
+|gpu - oracle| <= 2e-2 for INT8 caches (the oracle on the dequantised cache)."""
 
 import numpy as np
 import pytest
@@ -33,8 +34,15 @@ def run_mq(g, q, cu_q, max_q, num_parts=0):
     ws = torch.empty(B.pkv_multiquery_workspace_size(cfg.batch, cfg.num_q_heads, max_q, g.k_cache,
                                                      num_parts), dtype=torch.uint8, device="cuda")
     B.pkv_multiquery_attn(qd, cu, max_q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
-                          cfg.softmax_scale, out, ws, num_parts, g.status)
+                          cfg.softmax_scale, out, ws, num_parts, g.status, k_scales=g.k_scales,
+                          v_scales=g.v_scales)
     return out
+
+
+def want_mq(w, o, seqs=None):
+    return oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
+                                             w.context_lens, w.cfg.softmax_scale, o.ks, o.vs,
+                                             seqs=seqs)
 
 
 SMALL = {
@@ -47,6 +55,17 @@ SMALL = {
                          kv_dtype="f16", q_dtype="f16", src_dtype="f16", q_len=9,
                          len_groups=((6, 9, 500),)),
     "g4_q1": variant(CONFIGS["gqa8b"], batch=9, len_groups=((9, 1, 700),)),
+    # group 8 (64 q / 8 kv heads)
+    "g8_q5": variant(CONFIGS["gqa70b"], batch=8, q_len=5, len_groups=((8, 5, 800),)),
+    # INT8 caches (the mma.sync kernel with codes entering as fp16 carriers)
+    "int8_q5": variant(CONFIGS["spec_verify_int8"], batch=12, len_groups=((12, 5, 900),)),
+    "int8_q9_d64_f16": variant(CONFIGS["spec_verify_int8"], batch=6, num_q_heads=8,
+                               num_kv_heads=4, head_dim=64, q_dtype="f16", src_dtype="f16",
+                               q_len=9, len_groups=((6, 9, 500),)),
+    "int8_g8_q3": variant(CONFIGS["spec_verify_int8"], batch=6, num_q_heads=64, q_len=3,
+                          len_groups=((6, 3, 600),)),
+    "int8_g1_q2": variant(CONFIGS["spec_verify_int8"], batch=5, num_q_heads=4, num_kv_heads=4,
+                          q_len=2, len_groups=((5, 2, 400),)),
 }
 _cache = {}
 
@@ -55,9 +74,7 @@ def case(name):
     if name not in _cache:
         w = make_workload(SMALL[name])
         g, o = GpuCase(w), OracleCase(w)
-        want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
-                                                 w.context_lens, w.cfg.softmax_scale)
-        _cache[name] = (w, g, o, want)
+        _cache[name] = (w, g, o, want_mq(w, o))
     return _cache[name]
 
 
@@ -67,7 +84,7 @@ def test_multiquery_small(name, parts):
     w, g, o, want = case(name)
     out = run_mq(g, w.q, w.cu_q, w.cfg.q_len, parts)
     _sync()
-    assert_attention_close(out_to_f64(out), want, False, f"{name} parts={parts}")
+    assert_attention_close(out_to_f64(out), want, w.cfg.kv_dtype == "i8", f"{name} parts={parts}")
     assert int(g.status.item()) == 0
 
 
@@ -99,23 +116,23 @@ def test_variable_query_counts_including_empty():
         assert_attention_close(out_to_f64(out), want, False, f"varlen parts={parts}")
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "i8"])
 @pytest.mark.parametrize("n", [48, 33])
 def test_first_prefill_chunk_from_position_zero(dtype, n):
     """The whole context is new (L == n): query i sees only tokens 0..i, so
     the first rows average two or three values and expose any rounding of
-    the probabilities."""
+    the probabilities (INT8: a bf16 q over an INT8 cache)."""
+    qd = "bf16" if dtype == "i8" else dtype
     cfg = variant(CONFIGS["prefill_chunk"], batch=4, q_len=n, max_len=64,
-                  len_groups=((4, n, n),), kv_dtype=dtype, q_dtype=dtype, src_dtype=dtype)
+                  len_groups=((4, n, n),), kv_dtype=dtype, q_dtype=qd, src_dtype=qd)
     w = make_workload(cfg)
     assert (w.context_lens == n).all()
     g, o = GpuCase(w), OracleCase(w)
-    want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
-                                             w.context_lens, w.cfg.softmax_scale)
+    want = want_mq(w, o)
     for parts in (0, 5):
         out = run_mq(g, w.q, w.cu_q, n, parts)
         _sync()
-        assert_attention_close(out_to_f64(out), want, False, f"{dtype} from 0 parts={parts}")
+        assert_attention_close(out_to_f64(out), want, dtype == "i8", f"{dtype} from 0 parts={parts}")
 
 
 # Query runs that fill 128-row tiles (q_len * g >= 128) take the tcgen05 kernel.
@@ -130,6 +147,8 @@ TC = {
     # scores spread over a wide range: running maxima jump by more than 2^8
     "g4_wide_scores": variant(CONFIGS["prefill_chunk"], batch=2, q_len=40, max_len=1500,
                               len_groups=((2, 40, 1500),), q_std=6.0),
+    "g8_d128_bf16": variant(CONFIGS["prefill_chunk"], batch=2, num_q_heads=64, q_len=40,
+                            max_len=900, len_groups=((2, 40, 900),)),
 }
 
 
@@ -146,6 +165,21 @@ def test_tensor_core_row_tiles(name):
     got = out_to_f64(out)
     assert np.isfinite(got).all()
     assert_attention_close(got, want, False, name)
+    assert int(g.status.item()) == 0
+
+
+def test_long_query_runs_over_an_int8_cache():
+    """Query runs that would fill 128-row tiles: over an INT8 cache the
+    mma.sync kernel serves them (the tcgen05 kernel takes 16-bit operands)."""
+    cfg = variant(CONFIGS["spec_verify_int8"], batch=3, q_len=64, max_len=1500,
+                  len_groups=((3, 64, 1500),))
+    w = make_workload(cfg)
+    g, o = GpuCase(w), OracleCase(w)
+    want = want_mq(w, o)
+    for parts in (0, 7):
+        out = run_mq(g, w.q, w.cu_q, cfg.q_len, parts)
+        _sync()
+        assert_attention_close(out_to_f64(out), want, True, f"int8 q_len 64 parts={parts}")
     assert int(g.status.item()) == 0
 
 
@@ -195,7 +229,7 @@ def test_too_many_queries_are_flagged_not_written():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["spec_verify", "prefill_chunk"])
+@pytest.mark.parametrize("name", ["spec_verify", "prefill_chunk", "spec_verify_int8"])
 def test_multiquery_full_size_sampled(name):
     w = make_workload(CONFIGS[name])
     g, o = GpuCase(w), OracleCase(w)
@@ -203,12 +237,11 @@ def test_multiquery_full_size_sampled(name):
     order = np.argsort(lens)
     seqs = sorted(set(order[:2].tolist() + order[-2:].tolist() +
                       np.linspace(0, w.cfg.batch - 1, min(8, w.cfg.batch)).astype(int).tolist()))
-    want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables, lens,
-                                             w.cfg.softmax_scale, seqs=seqs)
+    want = want_mq(w, o, seqs=seqs)
     out = run_mq(g, w.q, w.cu_q, w.cfg.q_len)
     _sync()
     got = out_to_f64(out)
     rows = np.concatenate([np.arange(w.cu_q[b], w.cu_q[b + 1]) for b in seqs])
-    assert_attention_close(got[rows], want, False, name)
+    assert_attention_close(got[rows], want, w.cfg.kv_dtype == "i8", name)
     assert np.isfinite(got).all()
     assert int(g.status.item()) == 0
