@@ -129,18 +129,29 @@ class OracleCase:
                                              self.ks, self.vs, seqs=seqs)
 
 
+def error_figures(got, want):
+    """max |g - o| and max |g - o| / |o| over the elements with |o| >= 0.2."""
+    err = np.abs(got - want)
+    big = np.abs(want) >= 0.2
+    rel = float((err[big] / np.abs(want[big])).max()) if big.any() else 0.0
+    return float(err.max()) if err.size else 0.0, rel
+
+
 def assert_attention_close(got, want, int8: bool, what=""):
+    """Element-wise bound (bf16 / fp16 KV: 2e-3 + 1e-2 |o|; INT8: 2e-2);
+    returns (max abs error, max relative error where |o| >= 0.2)."""
     err = np.abs(got - want)
     if int8:
         bad = err > TOL_I8
     else:
         bad = err > TOL_ABS + TOL_REL * np.abs(want)
+    max_abs, max_rel = error_figures(got, want)
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance, first at "
                              f"{tuple(i)}: got {got[tuple(i)]!r} want {want[tuple(i)]!r}; "
-                             f"max abs err {err.max():.3e}")
-    return float(err.max())
+                             f"max abs err {max_abs:.3e}, max rel err (|o| >= 0.2) {max_rel:.3e}")
+    return max_abs, max_rel
 
 
 def workload(cfg):

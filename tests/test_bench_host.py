@@ -188,3 +188,15 @@ def test_reference_arm_other_ranks_do_no_work(capsys, monkeypatch):
     bench.run_reference(bench.parse_args(["--impl", "reference", "--config", "tiny",
                                           "--steps", "2", "--warmup", "3"]))
     assert capsys.readouterr().out == ""
+
+
+def test_error_figures_of_the_test_helper():
+    from _pkv_helpers import assert_attention_close, error_figures
+    want = np.array([1.0, -0.5, 0.1, 0.0, 0.25])
+    got = want + np.array([1e-3, -2e-3, 1e-3, 1e-3, 0.0])
+    max_abs, max_rel = error_figures(got, want)
+    assert abs(max_abs - 2e-3) < 1e-12 and abs(max_rel - 4e-3) < 1e-12   # 2e-3 / 0.5
+    assert assert_attention_close(got, want, False) == (max_abs, max_rel)
+    with pytest.raises(AssertionError):
+        assert_attention_close(want + 3e-3, want, False)        # 3e-3 > 2e-3 + 1e-2 * 0
+    assert assert_attention_close(want + 1e-2, want, True)[0] < 2e-2
