@@ -832,6 +832,7 @@ struct CombineParams {
     const int32_t* ws_prefix;
     void* out;
     int batch, hq, hkv, workers;
+    int segs_per_cta;     // segments (sequence, kv head) each CTA looks after
 };
 
 // Worker whose range holds unit u: the largest w with floor(w*U/W) <= u.
@@ -840,6 +841,8 @@ __device__ __forceinline__ long long worker_of(long long u, long long U, long lo
 }
 
 constexpr int kCombineThreads = 256;
+// Resident combine CTAs per SM (a full SM of threads: at most 32 registers).
+constexpr int kCombineCtasPerSm = 8;
 
 // Fold one partial state (m, l, o) into a running merge (M, den, num), all in
 // base 2: the running sums are rescaled when the maximum grows.
@@ -857,42 +860,22 @@ __device__ __forceinline__ void merge_state(float& M, float& den, float4& num, f
     num.x += a * o.x; num.y += a * o.y; num.z += a * o.z; num.w += a * o.w;
 }
 
-// One CTA per segment (sequence b, kv head): merge the pieces' states
+// Merge the pieces wf..wl of segment seg (sequence b, kv head kvh):
 // out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i (scores are in log2
-// units), or write zeros for an empty sequence. Segments finished inside one
-// worker were written by the split kernel and are skipped. The CTA's threads
-// form GROUPS groups of G*D/4 threads (one float4 of output each); group k
-// merges pieces k, k + GROUPS, ... and the groups are merged in shared memory.
+// units). The CTA's threads form GROUPS groups of G*D/4 threads (one float4 of
+// output each): group k merges pieces k, k + GROUPS, ... and the groups merge
+// in shared memory. Every thread of the CTA calls it with the same segment.
 template <typename QT, int D, int G>
-__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const CombineParams c) {
+__device__ __forceinline__ void merge_segment(const CombineParams& c, long long seg, int b, int kvh,
+                                              int wf, int wl, float* s_m, float* s_den,
+                                              float4* s_num) {
     constexpr int Q = D / 4, ITEMS = G * Q, GROUPS = kCombineThreads / ITEMS;
-    static_assert(kCombineThreads % ITEMS == 0, "item layout");
-    __shared__ float s_m[kCombineThreads], s_den[kCombineThreads];
-    __shared__ float4 s_num[kCombineThreads];
-    griddep_wait();                 // partials come from the split grid
-    const int seg = blockIdx.x;
-    const int b = seg / c.hkv, kvh = seg - b * c.hkv;
-    const int* P = c.ws_prefix;
-    const int nb = P[b + 1] - P[b];
     const int t = threadIdx.x, item = t % ITEMS, grp = t / ITEMS;
     const int h = item / Q, d4 = item - h * Q;
-    const long long obase = ((long long)b * c.hq + kvh * G + h) * D + d4 * 4;
-    if (nb == 0) {
-        if (grp == 0) {
-            const float2 z[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            store_out<QT, 4>(c.out, obase, z, 0.f);
-        }
-        return;
-    }
-    const long long U = (long long)P[c.batch] * c.hkv;
-    const long long W = eff_workers(U, c.workers);
-    const long long uf = (long long)c.hkv * P[b] + (long long)kvh * nb;
-    const long long wf = worker_of(uf, U, W), wl = worker_of(uf + nb - 1, U, W);
-    if (wf == wl) return;
     float M = -INFINITY, den = 0.f;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (long long w = wf + grp; w <= wl; w += GROUPS) {
+    for (int w = wf + grp; w <= wl; w += GROUPS) {
         const long long slot = seg + w;
         const float2 ml = *reinterpret_cast<const float2*>(c.part_ml + (slot * G + h) * 2);
         const float4 o = *reinterpret_cast<const float4*>(c.part_o + (slot * G + h) * D + d4 * 4);
@@ -903,20 +886,110 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
         s_den[t] = den;
         s_num[t] = num;
         __syncthreads();
-        if (grp != 0) return;
+        if (grp == 0) {
 #pragma unroll
-        for (int k = 1; k < GROUPS; ++k) {
-            const int o = k * ITEMS + item;
-            // s_num holds unnormalised sums relative to s_m: merge as a state
-            merge_state(M, den, num, s_m[o], s_den[o], s_num[o]);
+            for (int k = 1; k < GROUPS; ++k) {
+                const int o = k * ITEMS + item;
+                // s_num holds unnormalised sums relative to s_m: merge as a state
+                merge_state(M, den, num, s_m[o], s_den[o], s_num[o]);
+            }
         }
     }
-    const float inv = den > 0.f ? 1.0f / den : 0.f;
-    const float2 v[2] = {make_float2(num.x, num.y), make_float2(num.z, num.w)};
-    store_out<QT, 4>(c.out, obase, v, inv);
+    if (grp == 0) {
+        const long long obase = ((long long)b * c.hq + kvh * G + h) * D + d4 * 4;
+        const float inv = den > 0.f ? 1.0f / den : 0.f;
+        const float2 v[2] = {make_float2(num.x, num.y), make_float2(num.z, num.w)};
+        store_out<QT, 4>(c.out, obase, v, inv);
+    }
+}
+
+// Zero row for the empty sequence b, kv head kvh.
+template <typename QT, int D, int G>
+__device__ __forceinline__ void zero_segment(const CombineParams& c, int b, int kvh) {
+    constexpr int Q = D / 4, ITEMS = G * Q;
+    const int t = threadIdx.x, item = t % ITEMS;
+    const int h = item / Q, d4 = item - h * Q;
+    if (t < ITEMS) {
+        const float2 z[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        store_out<QT, 4>(c.out, ((long long)b * c.hq + kvh * G + h) * D + d4 * 4, z, 0.f);
+    }
+}
+
+// One CTA per segment (sequence b, kv head): write zeros for an empty
+// sequence, merge the pieces of a segment split over several workers, and
+// leave segments finished inside one worker (written by the split kernel)
+// alone. Used while the grid is at most two waves of resident CTAs.
+template <typename QT, int D, int G>
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const CombineParams c) {
+    __shared__ float s_m[kCombineThreads], s_den[kCombineThreads];
+    __shared__ float4 s_num[kCombineThreads];
+    griddep_wait();                 // partials come from the split grid
+    const int seg = blockIdx.x;
+    const int b = seg / c.hkv, kvh = seg - b * c.hkv;
+    const int* P = c.ws_prefix;
+    const int nb = P[b + 1] - P[b];
+    if (nb == 0) {
+        zero_segment<QT, D, G>(c, b, kvh);
+        return;
+    }
+    const long long U = (long long)P[c.batch] * c.hkv;
+    const long long W = eff_workers(U, c.workers);
+    const long long uf = (long long)c.hkv * P[b] + (long long)kvh * nb;
+    // workers are below 2^31 (the host caps them)
+    const int wf = int(worker_of(uf, U, W)), wl = int(worker_of(uf + nb - 1, U, W));
+    if (wf == wl) return;
+    merge_segment<QT, D, G>(c, seg, b, kvh, wf, wl, s_m, s_den, s_num);
     // Only now may the next grid start launching: a decode split launched
     // early here would take SM resources while this grid still runs, which
     // measured ~30 % slower steps.
+    griddep_launch_dependents();
+}
+
+// Large batches: each CTA looks after a run of segs_per_cta consecutive
+// segments, so that the grid stays about two waves deep however many
+// segments there are (per-CTA overhead, not merging, is what grows with the
+// batch). Every warp checks the run 32 segments at a time, one per lane; the
+// ballot of the lanes' answers gives all warps the same list of segments to
+// zero or merge, so the CTA needs no shared list and no barrier to agree on
+// it. Split segments number at most one per worker boundary.
+template <typename QT, int D, int G>
+__global__ void __launch_bounds__(kCombineThreads, kCombineCtasPerSm)
+decode_combine_runs_kernel(const CombineParams c) {
+    __shared__ float s_m[kCombineThreads], s_den[kCombineThreads];
+    __shared__ float4 s_num[kCombineThreads];
+    griddep_wait();                 // partials come from the split grid
+    const int* P = c.ws_prefix;
+    const long long U = (long long)P[c.batch] * c.hkv;
+    const long long W = eff_workers(U, c.workers);
+    const int lane = threadIdx.x & 31;
+    const int S = c.batch * c.hkv;                     // < 2^31: checked on the host
+    const int seg0 = int(blockIdx.x) * c.segs_per_cta;
+    for (int base = 0; base < c.segs_per_cta; base += 32) {
+        bool split = false, empty = false;
+        if (base + lane < c.segs_per_cta && seg0 + base + lane < S) {
+            const int seg = seg0 + base + lane;
+            const int b = seg / c.hkv, kvh = seg - b * c.hkv;
+            const int nb = P[b + 1] - P[b];
+            const long long uf = (long long)c.hkv * P[b] + (long long)kvh * nb;
+            empty = nb == 0;
+            split = !empty && worker_of(uf, U, W) != worker_of(uf + nb - 1, U, W);
+        }
+        const unsigned empties = __ballot_sync(0xffffffffu, empty);
+        for (unsigned todo = __ballot_sync(0xffffffffu, split) | empties; todo; todo &= todo - 1) {
+            const int j = __ffs(todo) - 1;
+            const int seg = seg0 + base + j;
+            const int b = seg / c.hkv, kvh = seg - b * c.hkv;
+            if ((empties >> j) & 1u) {
+                zero_segment<QT, D, G>(c, b, kvh);
+                continue;
+            }
+            const int nb = P[b + 1] - P[b];
+            const long long uf = (long long)c.hkv * P[b] + (long long)kvh * nb;
+            merge_segment<QT, D, G>(c, seg, b, kvh, int(worker_of(uf, U, W)),
+                                    int(worker_of(uf + nb - 1, U, W)), s_m, s_den, s_num);
+            __syncthreads();   // the next segment reuses s_m / s_den / s_num
+        }
+    }
     griddep_launch_dependents();
 }
 
@@ -948,7 +1021,11 @@ struct Impl {
                    smem, st, p);
     }
     static void combine(const CombineParams& c, int grid, cudaStream_t st) {
-        launch_pdl(decode_combine_kernel<QT, D, G>, dim3(grid), dim3(kCombineThreads), 0, st, c);
+        if (c.segs_per_cta == 1)
+            launch_pdl(decode_combine_kernel<QT, D, G>, dim3(grid), dim3(kCombineThreads), 0, st, c);
+        else
+            launch_pdl(decode_combine_runs_kernel<QT, D, G>, dim3(grid), dim3(kCombineThreads), 0,
+                       st, c);
     }
     // 16-bit caches at D = 128 default to 2 CTAs (8 worker warps) per SM
     // although 3 fit: on the GQA-8B workload the split kernel read 6.74 TB/s
@@ -1104,7 +1181,14 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
         c.ws_prefix = reinterpret_cast<const int32_t*>(ws + l.prefix_off);
         c.out = out;
         c.batch = batch; c.hq = hq; c.hkv = hkv; c.workers = int(workers);
-        ops.combine(c, batch * hkv, stream);
+        // One segment per CTA up to two waves of resident combine CTAs
+        // (152 SMs x 8); beyond that, runs of segments keep the grid at about
+        // two waves.
+        const long long segs = (long long)batch * hkv;
+        long long spc = (segs + 2431) / 2432;
+        spc = spc < 1 ? 1 : (spc > kCombineThreads ? kCombineThreads : spc);
+        c.segs_per_cta = int(spc);
+        ops.combine(c, int((segs + spc - 1) / spc), stream);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;

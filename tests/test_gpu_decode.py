@@ -112,16 +112,25 @@ def test_empty_and_single_token_sequences():
         assert_attention_close(got, want, False, f"tiny lengths parts={parts}")
 
 
-def test_large_batch_short_sequences():
-    """Batch 8192 (the largest supported) of 1..40-token sequences."""
-    cfg = variant(CONFIGS["gqa8b"], batch=8192, len_groups=((8192, 1, 40),), max_len=64)
+@pytest.mark.parametrize("parts", [0, 37])
+def test_large_batch_short_sequences(parts):
+    """Batch 8192 (the largest supported) of 0..40-token sequences.
+
+    At this batch each combine CTA looks after a run of segments, some empty
+    and some split over two workers; every 7th sequence is checked.
+    """
+    cfg = variant(CONFIGS["gqa8b"], batch=8192, len_groups=((1024, 0, 0), (7168, 1, 40)),
+                  max_len=64)
     w = make_workload(cfg)
+    assert (w.context_lens == 0).sum() >= 1024
     g = GpuCase(w)
-    seqs = list(range(0, 8192, 97)) + [8191]
+    seqs = list(range(0, 8192, 7)) + [8191]
     want = OracleCase(w).attention(seqs=seqs)
-    out, _ = g.decode()
+    out, _ = g.decode(num_parts=parts)
     _sync()
-    assert_attention_close(out_to_f64(out)[seqs], want, False, "batch 8192")
+    got = out_to_f64(out)
+    assert np.all(got[w.context_lens == 0] == 0)
+    assert_attention_close(got[seqs], want, False, f"batch 8192 parts={parts}")
 
 
 def test_stale_nan_rows_are_never_read():
