@@ -50,6 +50,15 @@ __device__ __forceinline__ uint4 sel4(bool c, const uint4& a, const uint4& b) {
     return make_uint4(c ? a.x : b.x, c ? a.y : b.y, c ? a.z : b.z, c ? a.w : b.w);
 }
 
+// The block prefix kept in shared memory has at most kPrefixEntries + 1
+// entries, so that its size does not grow with the batch: up to
+// kPrefixEntries sequences it is exact (stride 1); beyond, it holds every
+// stride-th entry, stride = ceil(batch / kPrefixEntries), and a lookup ends
+// with a scan of at most stride context lengths.
+constexpr int kPrefixEntries = 256;
+// Largest shared-memory prefix area (scan scratch + prefix), any batch.
+constexpr int kPrefixMaxBytes = align_up(4 * kMaxWarpsPerCta + 4 * (kPrefixEntries + 1), 128);
+
 template <typename KV, int D, int G>
 struct Cfg {
     static constexpr int esize = Elem<KV>::bytes;
@@ -78,11 +87,12 @@ struct Cfg {
     static constexpr int WARP_BYTES = align_up(OFF_Q + NS * QBYTES, 128);
     // Worker warps per CTA: 4 (three CTAs share an SM); INT8 units take more
     // shared memory than three 4-warp CTAs can have, so INT8 runs CTAs of 6
-    // warps, two per SM (228 KB of shared memory, 1 KB reserved per CTA),
-    // whenever a batch of 256 still fits, which keeps 12 warps per SM.
+    // warps, two per SM (228 KB of shared memory, 1 KB reserved per CTA, and
+    // the block prefix, at most kPrefixMaxBytes at any batch), which keeps 12
+    // warps per SM.
     static constexpr int kSmemPerSm = 233472, kReservedPerCta = 1024;
     static constexpr int WARPS =
-        (kI8 && 2 * (6 * WARP_BYTES + 1152 + kReservedPerCta) <= kSmemPerSm) ? 6 : 4;
+        (kI8 && 2 * (6 * WARP_BYTES + kPrefixMaxBytes + kReservedPerCta) <= kSmemPerSm) ? 6 : 4;
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int MIN_CTAS = WARPS == 6 ? 2 : 3;   // launch bounds: registers per thread
     static_assert(NS >= 2 && NS <= 32, "stage count (one parity bit per stage)");
@@ -90,10 +100,17 @@ struct Cfg {
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size (heads fill <= 8 MMA columns)");
 };
 
+__host__ __device__ inline int prefix_stride(int batch) {
+    return batch <= kPrefixEntries ? 1 : (batch + kPrefixEntries - 1) / kPrefixEntries;
+}
+__host__ __device__ inline int prefix_chunks(int batch) {
+    const int st = prefix_stride(batch);
+    return (batch + st - 1) / st;
+}
 // Dynamic shared memory starts with kMaxWarpsPerCta ints of scan scratch, then
-// the block prefix [batch + 1]; the per-warp regions follow, 128-byte aligned.
+// the block prefix [chunks + 1]; the per-warp regions follow, 128-byte aligned.
 __host__ __device__ inline int prefix_bytes(int batch) {
-    return align_up(4 * kMaxWarpsPerCta + 4 * (batch + 1), 128);
+    return align_up(4 * kMaxWarpsPerCta + 4 * (prefix_chunks(batch) + 1), 128);
 }
 
 // Workers that get units: at most one per kMinUnits units, so every range is
@@ -135,8 +152,16 @@ __device__ __forceinline__ int clamp_len(int L, int mb, uint32_t* status, bool f
     return L;
 }
 
-// prefix[b] = sum_{b' < b} ceil(L_b' / UT) for b in [0, batch], UT = tokens
-// per unit (16 UB); all threads.
+// Units (UT tokens each) of sequence b, from its clamped length.
+template <int UT>
+__device__ __forceinline__ int seq_units(const DecodeParams& p, int b) {
+    return (clamp_len(__ldg(p.context_lens + b), p.mb, p.status, false) + UT - 1) / UT;
+}
+
+// Block prefix P[b] = sum_{b' < b} ceil(L_b' / UT) for b in [0, batch], UT =
+// tokens per unit (16 UB); all threads. Shared memory keeps prefix[c] =
+// P[c * stride] for c in [0, chunks) and prefix[chunks] = P[batch]; CTA 0
+// writes the whole of P to ws_prefix for the combine.
 template <int UT, int NT>
 __device__ void build_prefix(const DecodeParams& p, int* warp_tot, int* prefix) {
     const int t = threadIdx.x;
@@ -159,28 +184,57 @@ __device__ void build_prefix(const DecodeParams& p, int* warp_tot, int* prefix) 
     int base = 0;
     for (int w = 0; w < warp; ++w) base += warp_tot[w];
     int run = base + inc - sum;
+    const int stride = prefix_stride(p.batch);
+    if (stride == 1) {
+        for (int i = lo; i < hi; ++i) {
+            prefix[i] = run;
+            run += (clamp_len(p.context_lens[i], p.mb, p.status, false) + UT - 1) / UT;
+        }
+        if (t == NT - 1) prefix[p.batch] = run;
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int i = t; i <= p.batch; i += NT) p.ws_prefix[i] = prefix[i];
+        return;
+    }
     for (int i = lo; i < hi; ++i) {
-        prefix[i] = run;
+        if (i % stride == 0) prefix[i / stride] = run;
+        if (blockIdx.x == 0) p.ws_prefix[i] = run;
         run += (clamp_len(p.context_lens[i], p.mb, p.status, false) + UT - 1) / UT;
     }
-    if (t == NT - 1) prefix[p.batch] = run;
+    if (t == NT - 1) {
+        prefix[prefix_chunks(p.batch)] = run;
+        if (blockIdx.x == 0) p.ws_prefix[p.batch] = run;
+    }
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int i = t; i <= p.batch; i += NT) p.ws_prefix[i] = prefix[i];
 }
 
 // Unit u -> (b, kv head, unit j of the segment, i.e. blocks UB j .. UB j + UB - 1):
-// b is the last sequence whose first unit is <= u (it always has blocks,
-// since u < U).
-__device__ __forceinline__ void decode_unit(long long u, const int* prefix, int batch, int hkv,
+// b is the last sequence whose first unit is <= u (it always has units, since
+// u < U). A binary search finds the last prefix chunk starting at or before
+// u; with a strided prefix the chunk's sequences are then walked in order.
+template <int UT>
+__device__ __forceinline__ void decode_unit(long long u, const int* prefix, const DecodeParams& p,
                                             int& b, int& kvh, int& j) {
-    const int x = int(u / hkv);
+    const int x = int(u / p.hkv);
+    const int stride = prefix_stride(p.batch), chunks = prefix_chunks(p.batch);
     int lo = 0;
-    for (int step = 1 << 13; step; step >>= 1)  // kMaxBatch = 2^13
-        if (lo + step < batch && prefix[lo + step] <= x) lo += step;
-    b = lo;
-    const int nb = prefix[b + 1] - prefix[b];
-    const int r = int(u - (long long)hkv * prefix[b]);
+    static_assert(kPrefixEntries <= 256, "search width: lo reaches at most 255");
+    for (int step = 1 << 7; step; step >>= 1)
+        if (lo + step < chunks && prefix[lo + step] <= x) lo += step;
+    int first = prefix[lo], nb;
+    if (stride == 1) {
+        b = lo;
+        nb = prefix[lo + 1] - first;
+    } else {
+        b = lo * stride;
+        const int last = min(b + stride, p.batch) - 1;
+        nb = seq_units<UT>(p, b);
+        while (b < last && x >= first + nb) {   // ends inside the chunk since x < prefix[lo + 1]
+            first += nb;
+            nb = seq_units<UT>(p, ++b);
+        }
+    }
+    const int r = int(u - (long long)p.hkv * first);
     kvh = r / nb;
     j = r - kvh * nb;
 }
@@ -222,7 +276,7 @@ decode_split_kernel(const DecodeParams p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long w = (long long)blockIdx.x * C::WARPS + warp;
-    const long long U = (long long)prefix[p.batch] * p.hkv;
+    const long long U = (long long)prefix[prefix_chunks(p.batch)] * p.hkv;
     const long long W = eff_workers(U, p.workers);
     if (w >= W || U == 0) return;
     const long long u0 = w * U / W, u1 = (w + 1) * U / W;
@@ -246,7 +300,7 @@ decode_split_kernel(const DecodeParams p) {
         const long long u = base + lane;
         blk1 = -1;
         if (u < u1) {
-            decode_unit(u, prefix, p.batch, p.hkv, b, kvh, j);
+            decode_unit<C::UT>(u, prefix, p, b, kvh, j);
             const int32_t* row = p.block_tables + (long long)b * p.mb + C::UB * j;
             blk = __ldg(row);
             len = clamp_len(__ldg(p.context_lens + b), p.mb, p.status, false);
@@ -393,7 +447,7 @@ decode_split_kernel(const DecodeParams p) {
     float pv[2] = {0.f, 0.f};                    // INT8: sum_t P_t of this lane's tokens
 
     auto finalize = [&]() {
-        const int nbk = prefix[pb + 1] - prefix[pb];
+        const int nbk = (plen + C::UT - 1) / C::UT;   // plen: pb's clamped length
         const long long seg = (long long)pb * p.hkv + pkvh;
         const bool whole = (first_j == 0 && last_j == nbk - 1);
         float lh[2] = {lsum[0], lsum[1]};

@@ -133,6 +133,26 @@ def test_large_batch_short_sequences(parts):
     assert_attention_close(got[seqs], want, False, f"batch 8192 parts={parts}")
 
 
+@pytest.mark.parametrize("base,parts", [("gqa8b", 0), ("gqa8b", 501), ("gqa8b_int8", 0),
+                                        ("gqa8b_int8", 77)])
+def test_batch_above_the_exact_prefix(base, parts):
+    """1001 sequences: the split kernel keeps every 4th block-prefix entry in
+    shared memory (251 chunks, the last holding one sequence) and walks the
+    rest; runs of empty sequences cover whole chunks. Every sequence is
+    checked."""
+    cfg = variant(CONFIGS[base], batch=1001, max_len=320,
+                  len_groups=((300, 1, 200), (20, 0, 0), (400, 1, 300), (281, 0, 50)))
+    w = make_workload(cfg)
+    g = GpuCase(w)
+    want = OracleCase(w).attention()
+    out, _ = g.decode(num_parts=parts)
+    _sync()
+    got = out_to_f64(out)
+    assert int(g.status.item()) == 0
+    assert np.all(got[w.context_lens == 0] == 0)
+    assert_attention_close(got, want, cfg.kv_dtype == "i8", f"batch 1001 {base} parts={parts}")
+
+
 def test_stale_nan_rows_are_never_read():
     """Rows past each context hold NaN; the output must stay finite and right."""
     w, g, want = case("gqa8b")

@@ -9,11 +9,14 @@ partial state per range at slot ``segment + worker``, and the combine finds a
 segment's ranges as ``worker_of(first unit) .. worker_of(last unit)`` minus
 empty ranges. This restates that index arithmetic in Python and checks, for
 random batches, that every unit is decoded back to itself, that the combine
-visits exactly the workers that wrote pieces, and that slots never collide.
+visits exactly the workers that wrote pieces, and that slots never collide;
+and that the lookup over the strided block prefix used above 256 sequences
+finds the same sequence as the exact prefix.
 The multi-query split's partition (row tiles over the blocks their queries
 can see) is checked the same way.
 """
 
+import bisect
 import random
 
 
@@ -55,6 +58,54 @@ def test_partition_slots_and_combine_ranges():
                     assert seg + w not in slots and seg + w < B * hkv + W
                     slots.add(seg + w)
 
+
+
+PREFIX_ENTRIES = 256   # shared-memory block prefix entries of the decode split
+
+
+def strided_lookup(x, coarse, stride, nblk):
+    """The split kernel's unit lookup over a strided prefix: the last chunk
+    whose first sequence starts at or before x, then a walk over its
+    sequences. Returns (b, first unit of b, units of b)."""
+    lo = 0
+    step = 128
+    while step:
+        if lo + step < len(coarse) - 1 and coarse[lo + step] <= x:
+            lo += step
+        step >>= 1
+    first = coarse[lo]
+    b = lo * stride
+    last = min(b + stride, len(nblk)) - 1
+    nb = nblk[b]
+    while b < last and x >= first + nb:
+        first += nb
+        b += 1
+        nb = nblk[b]
+    return b, first, nb
+
+
+def test_strided_prefix_lookup_matches_exact_prefix():
+    """Above 256 sequences the kernel keeps every stride-th prefix entry in
+    shared memory and walks the rest; it must find the same sequence as the
+    exact prefix, through runs of empty sequences and a ragged last chunk."""
+    rng = random.Random(1)
+    for _ in range(60):
+        B = rng.choice([257, 300, 511, 1000, 1001, 4097, 8192])
+        stride = 1 if B <= PREFIX_ENTRIES else -(-B // PREFIX_ENTRIES)
+        chunks = -(-B // stride)
+        assert chunks <= PREFIX_ENTRIES
+        nblk = [rng.choice([0, 0, 1, 2, 5]) for _ in range(B)]
+        for _ in range(rng.randint(0, 4)):          # long empty runs
+            a = rng.randrange(B)
+            for i in range(a, min(B, a + rng.randint(1, 3 * stride))):
+                nblk[i] = 0
+        prefix = [0]
+        for n in nblk:
+            prefix.append(prefix[-1] + n)
+        coarse = [prefix[c * stride] for c in range(chunks)] + [prefix[B]]
+        for x in range(prefix[B]):
+            b = bisect.bisect_right(prefix, x) - 1   # the exact rule: last b with prefix[b] <= x
+            assert strided_lookup(x, coarse, stride, nblk) == (b, prefix[b], nblk[b])
 
 # ----------------------------------------------------- multi-query kernel ---
 # The multi-query split orders units (sequence b, kv head, row tile t, block j)
