@@ -113,13 +113,14 @@ __global__ void i8_gather_kernel(I8Args a) {
     const long long items = (long long)a.n_tokens * a.hkv;
     for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
          it += ((long long)gridDim.x * blockDim.x) >> 5) {
+        // the new rows are loaded while the slot is resolved
+        float xk[D / 32], xv[D / 32];
+        load_row<S, D>(a.k_new, it * D, xk);
+        load_row<S, D>(a.v_new, it * D, xv);
         long long n;
         int row;
         const long long t = item_tile(a, it, &n, &row, true);
         if (t < 0) continue;
-        float xk[D / 32], xv[D / 32];
-        load_row<S, D>(a.k_new, it * D, xk);
-        load_row<S, D>(a.v_new, it * D, xv);
         float mk = 0.f, mv = 0.f;
 #pragma unroll
         for (int e = 0; e < D / 32; ++e) {
@@ -149,8 +150,41 @@ __device__ __forceinline__ float settle_scale(uint32_t amax_bits, float s_o, boo
     return (s_o != 0.f && s_c <= s_o) ? s_o : s_c;
 }
 
+__device__ __forceinline__ uint4 requant_vec(const uint4& in, float s_o, float s) {
+    return make_uint4(requant_word(in.x, s_o, s), requant_word(in.y, s_o, s),
+                      requant_word(in.z, s_o, s), requant_word(in.w, s_o, s));
+}
+
+template <int EPL>
+__device__ __forceinline__ void store_codes(int8_t* cache, long long dst, const float* x, float s) {
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) packed |= (uint32_t(quant_code(x[e], s)) & 0xffu) << (8 * e);
+    if (EPL == 4) *reinterpret_cast<uint32_t*>(cache + dst) = packed;
+    else *reinterpret_cast<uint16_t*>(cache + dst) = uint16_t(packed);
+}
+
+// Re-express every stored code of one tile under a grown scale: each lane
+// loads all its 16-byte words before storing any, so the tile costs one
+// memory round trip.
+template <int D>
+__device__ __forceinline__ void requant_tile(int8_t* tile, float s_o, float s, int lane) {
+    constexpr int V4 = kBlockSize * D / 16 / 32;   // 16-byte words of a tile per lane
+    uint4* w = reinterpret_cast<uint4*>(tile);
+    uint4 c[V4];
+#pragma unroll
+    for (int i = 0; i < V4; ++i) c[i] = w[lane + 32 * i];
+#pragma unroll
+    for (int i = 0; i < V4; ++i) w[lane + 32 * i] = requant_vec(c[i], s_o, s);
+}
+
+// One warp per tile (the warp of the call's first token in it) settles the
+// K and V scales, requantises a tile whose scale grew, and encodes the call's
+// new rows under the final scales. The first new row and the stored scales
+// are loaded together, before the scales are settled, to shorten the chain
+// of dependent memory accesses.
 template <typename S, int D>
-__global__ void i8_settle_kernel(I8Args a) {
+__global__ void __launch_bounds__(kThreads, 4) i8_settle_kernel(I8Args a) {
     griddep_wait();
     griddep_launch_dependents();
     constexpr int EPL = D / 32;
@@ -166,37 +200,37 @@ __global__ void i8_settle_kernel(I8Args a) {
         const TileScratch sc = *ts;
         if (sc.owner != uint32_t(a.n_tokens - n)) continue;   // one warp per tile
         const int kvh = int(t % a.hkv);
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-            int8_t* cache = kv ? a.v_cache : a.k_cache;
-            float* scales = kv ? a.v_scales : a.k_scales;
-            const float s_o = scales[t];
-            bool grow;
-            const float s = settle_scale(kv ? sc.amax_v : sc.amax_k, s_o, &grow);
-            if (grow) {   // every stored code re-expressed under the grown scale
-                uint32_t* words = reinterpret_cast<uint32_t*>(cache + t * kBlockSize * D);
-                for (int w = lane; w < kBlockSize * D / 4; w += 32)
-                    words[w] = requant_word(words[w], s_o, s);
-            }
-            __syncwarp();
-            // the call's new rows of the tile, under the final scale
-            for (uint32_t m = sc.rows; m; m &= m - 1) {
-                const int r = __ffs(m) - 1;
-                const long long src = ((long long)a.row_tok[t * kBlockSize + r] * a.hkv + kvh) * D;
-                float x[EPL];
-                load_row<S, D>(kv ? a.v_new : a.k_new, src, x);
-                uint32_t packed = 0;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e)
-                    packed |= (uint32_t(quant_code(x[e], s)) & 0xffu) << (8 * e);
-                const long long dst = (t * kBlockSize + r) * D + lane * EPL;
-                if (EPL == 4) *reinterpret_cast<uint32_t*>(cache + dst) = packed;
-                else *reinterpret_cast<uint16_t*>(cache + dst) = uint16_t(packed);
-            }
-            if (lane == 0) scales[t] = s;
-        }
+        const float so_k = a.k_scales[t], so_v = a.v_scales[t];
+        // sc.rows holds at least this warp's own row
+        const int r0 = __ffs(sc.rows) - 1;
+        const long long src0 = ((long long)a.row_tok[t * kBlockSize + r0] * a.hkv + kvh) * D;
+        float xk[EPL], xv[EPL];
+        load_row<S, D>(a.k_new, src0, xk);
+        load_row<S, D>(a.v_new, src0, xv);
+        bool grow_k, grow_v;
+        const float sk = settle_scale(sc.amax_k, so_k, &grow_k);
+        const float sv = settle_scale(sc.amax_v, so_v, &grow_v);
+        if (grow_k) requant_tile<D>(a.k_cache + t * kBlockSize * D, so_k, sk, lane);
+        if (grow_v) requant_tile<D>(a.v_cache + t * kBlockSize * D, so_v, sv, lane);
         __syncwarp();
-        if (lane == 0) *ts = TileScratch{0u, 0u, 0u, 0u};   // zero again for the next call
+        const long long dst0 = (t * kBlockSize + r0) * D + lane * EPL;
+        store_codes<EPL>(a.k_cache, dst0, xk, sk);
+        store_codes<EPL>(a.v_cache, dst0, xv, sv);
+        // the call's other new rows of the tile
+        for (uint32_t m = sc.rows & (sc.rows - 1); m; m &= m - 1) {
+            const int r = __ffs(m) - 1;
+            const long long src = ((long long)a.row_tok[t * kBlockSize + r] * a.hkv + kvh) * D;
+            load_row<S, D>(a.k_new, src, xk);
+            load_row<S, D>(a.v_new, src, xv);
+            const long long dst = (t * kBlockSize + r) * D + lane * EPL;
+            store_codes<EPL>(a.k_cache, dst, xk, sk);
+            store_codes<EPL>(a.v_cache, dst, xv, sv);
+        }
+        if (lane == 0) {
+            a.k_scales[t] = sk;
+            a.v_scales[t] = sv;
+            *ts = TileScratch{0u, 0u, 0u, 0u};   // zero again for the next call
+        }
     }
 }
 
