@@ -769,14 +769,21 @@ def run_multiquery(args):
     tflops = flops / (attn_ms / 1e3) / 1e12
     # The library's dispatch rule: runs over fp16 / bf16 caches that fill
     # 128-row tiles (q_len x the group size) take the tcgen05 kernel, one
-    # launch; shorter runs and INT8 caches the mma.sync split kernel and its
-    # combine, two launches. Plus the append (two kernels for INT8).
+    # launch; runs of at most 24 rows over fp16 / bf16 caches the short-run
+    # split kernel and the combine, other runs and INT8 caches the mma.sync
+    # split kernel and the combine, two launches each. Plus the append (two
+    # kernels for INT8).
     g = cfg.num_q_heads // cfg.num_kv_heads
-    tc = nq * g >= 128 and cfg.kv_dtype != "i8"
-    kernel = "mq_tc_kernel" if tc else "mq_split_kernel"
+    rows = nq * g
+    if cfg.kv_dtype != "i8" and rows >= 128:
+        kernel, src = "mq_tc_kernel", ("mq_split.cuh", "mq.cu")
+    elif cfg.kv_dtype != "i8" and rows <= 24:
+        kernel, src = "mqt_split_kernel", ("mq_split.cuh", "mq_t.cu")
+    else:
+        kernel, src = "mq_split_kernel", ("mq_split.cuh",)
+    tc = kernel == "mq_tc_kernel"
     launches = (1 if tc else 2) + (2 if cfg.kv_dtype == "i8" else 1)
-    traffic = recorded_traffic(kernel, args.config,
-                               ("mq_split.cuh", "mq.cu") if tc else ("mq_split.cuh",))
+    traffic = recorded_traffic(kernel, args.config, src)
     # Bound: the workload's FLOP/byte against the machine balance (measured
     # tensor peak / measured HBM bandwidth). Long prefill chunks are dense
     # contractions; verification of a few draft tokens streams the cache.

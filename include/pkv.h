@@ -277,17 +277,22 @@ pkv_status pkv_merge_states(const float *part_m, const float *part_l, const floa
  * and the n_b queries form the rows of a tensor-core tile. Supported:
  * head_dim 64 or 128, g in {1, 2, 4, 8}, batch <= 4096. Workspace:
  * pkv_multiquery_workspace_size with the same batch, num_q_heads, max_q_len,
- * cache and num_parts (0 = one range per resident CTA); 256-byte aligned.
+ * cache and num_parts (0 = one range per resident worker); 256-byte aligned.
  * Caches 16-byte aligned.
- * Two kernels serve the call: for fp16 / bf16 caches, when max_q_len * g >=
- * 128 (a prefill chunk) and q, out are 16-byte aligned, a tcgen05 /
- * tensor-memory kernel with one CTA per (sequence, kv head, 128-row tile)
- * and no split (num_parts and the workspace are then not used, but are still
- * checked); otherwise, and for every INT8 cache, an mma.sync kernel whose
- * stream of units is cut into num_parts ranges and merged by a combine
- * kernel through the workspace. Both compute the same causal attention
- * within the same tolerance (INT8: within 2e-2 of attention over the
- * dequantised cache).
+ * Three kernels serve the call, by rows = max_q_len * g:
+ *  - fp16 / bf16 caches, rows >= 128 (a prefill chunk), q and out 16-byte
+ *    aligned: a tcgen05 / tensor-memory kernel with one CTA per (sequence,
+ *    kv head, 128-row tile) and no split (num_parts and the workspace are
+ *    then not used, but are still checked);
+ *  - fp16 / bf16 caches, rows <= 24 (speculative verification): an mma.sync
+ *    kernel with the rows on the MMA's N side, one warp per worker
+ *    (num_parts counts warps);
+ *  - otherwise, and for every INT8 cache: an mma.sync kernel with 16 rows
+ *    per warp, one CTA per worker.
+ * The split kernels cut their stream of units into num_parts ranges and a
+ * combine kernel merges the pieces through the workspace. All compute the
+ * same causal attention within the same tolerance (INT8: within 2e-2 of
+ * attention over the dequantised cache).
  * ------------------------------------------------------------------------ */
 size_t pkv_multiquery_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_q_len,
                                      const pkv_cache_desc *cache, int32_t num_parts);

@@ -43,14 +43,15 @@ pkv_status pkv_testing_decode_attn_stall(const void *q, pkv_dtype q_dtype,
                                          cudaStream_t stream);
 
 /* pkv_multiquery_attn (same arguments and checks) with the same two
- * changes, stall_cta naming a CTA of the kernel that serves the call: for
- * query runs served by the mma.sync split kernel, that CTA's first unit; for
- * runs served by the tcgen05 kernel, that CTA's first chunk never completes
- * (the tcgen05 kernel bounds its waits at 2 s whatever the limit given). After a stalled call *dev_status holds PKV_DEV_TIMEOUT plus a
- * diagnostic bit naming the waiting role (0x100 / 0x200: consumer /
- * producer of the split kernel; 0x400 / 0x800 / 0x1000: producer / MMA
- * issuer / softmax of the tcgen05 kernel); rows the stalled work covered are
- * undefined. */
+ * changes, stall_cta naming a worker of the kernel that serves the call: for
+ * query runs served by a split kernel, that worker's first unit (a CTA of the
+ * 16-rows-per-warp kernel, a warp of the short-run kernel); for runs served
+ * by the tcgen05 kernel, that CTA's first chunk never completes (the tcgen05
+ * kernel bounds its waits at 2 s whatever the limit given). After a stalled
+ * call *dev_status holds PKV_DEV_TIMEOUT plus a diagnostic bit naming the
+ * waiting role (0x100 / 0x200: consumer / producer of a split kernel;
+ * 0x400 / 0x800 / 0x1000: producer / MMA issuer / softmax of the tcgen05
+ * kernel); rows the stalled work covered are undefined. */
 pkv_status pkv_testing_multiquery_attn_stall(const void *q, pkv_dtype q_dtype,
                                              const int32_t *cu_q, int32_t max_q_len,
                                              const void *k_cache, const void *v_cache,

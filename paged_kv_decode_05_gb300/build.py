@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["append.cu", "decode.cu", "blocks.cu", "mq.cu", "mq_i8.cu", "merge.cu"]
+SOURCES = ["append.cu", "decode.cu", "blocks.cu", "mq.cu", "mq_i8.cu", "mq_t.cu", "merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -561,6 +561,10 @@ TcLaunch tc_pick(int D, int G) {
     return nullptr;
 }
 
+// Query rows per (sequence, kv head) up to which fp16 / bf16 caches take the
+// short-run kernel (mq_t.cu).
+constexpr long long kMqtMaxRows = 24;
+
 struct MqPlan {
     MqOps ops;
     int G, nw, tmax;
@@ -592,6 +596,8 @@ pkv_status mq_plan(const pkv_cache_desc* c, int batch, int hq, int max_q, pkv_dt
     bool ok;
     if (c->kv_dtype == PKV_I8)
         ok = mq_pick_i8(q_dtype, c->head_dim, pl->G, pl->nw, &pl->ops);
+    else if (rows <= kMqtMaxRows)   // short runs: rows on the MMA's N side, a warp per worker
+        ok = mqt_pick(c->kv_dtype, c->head_dim, pl->G, int((rows + 7) / 8), &pl->ops);
     else
         ok = c->kv_dtype == PKV_BF16 ? mq_pick_d<BF16, BF16>(c->head_dim, pl->G, pl->nw, &pl->ops)
                                      : mq_pick_d<F16, F16>(c->head_dim, pl->G, pl->nw, &pl->ops);
@@ -606,7 +612,7 @@ pkv_status mq_plan(const pkv_cache_desc* c, int batch, int hq, int max_q, pkv_dt
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             pl->ops.occupancy(&blocks, pl->smem) != cudaSuccess || blocks <= 0)
             return PKV_ERR_CUDA;
-        pl->workers = (long long)sms * blocks;
+        pl->workers = (long long)sms * blocks * pl->ops.wpc;
     }
     const long long slots = (long long)batch * c->num_kv_heads * pl->tmax + pl->workers;
     pl->ws_prefix = 0;
@@ -663,9 +669,12 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     if (!workspace || workspace_bytes < pl.ws_total || !mq_aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     const long long rows = (long long)cache->num_blocks * cache->num_kv_heads * kBlockSize;
-    CUtensorMap tk = {}, tv = {};   // INT8 tiles are read by 1-D bulk copies instead
-    if (!i8 && (!encode_cache_map(&tk, k_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows) ||
-                !encode_cache_map(&tv, v_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows)))
+    // INT8 tiles, and the tiles of the short-run kernel, are read by 1-D bulk
+    // copies instead of tensor maps
+    CUtensorMap tk = {}, tv = {};
+    if (!i8 && !pl.ops.raw &&
+        (!encode_cache_map(&tk, k_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows) ||
+         !encode_cache_map(&tv, v_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows)))
         return PKV_ERR_CUDA;
     // Query runs of 16-bit caches that fill 128-row tiles take the tcgen05
     // kernel (no split, no combine, no workspace); shorter runs, and every run
@@ -708,9 +717,11 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     p.stall_cta = stall_cta;
     if (pl.ops.prepare(pl.smem) != cudaSuccess) return PKV_ERR_CUDA;
     const MqI8Src ik{k_cache, k_scales}, iv{v_cache, v_scales};
-    const void* ks = i8 ? static_cast<const void*>(&ik) : static_cast<const void*>(&tk);
-    const void* vs = i8 ? static_cast<const void*>(&iv) : static_cast<const void*>(&tv);
-    if (pl.ops.split(ks, vs, p, int(pl.workers), pl.smem, stream) != cudaSuccess)
+    const bool raw = i8 || pl.ops.raw;
+    const void* ks = raw ? static_cast<const void*>(&ik) : static_cast<const void*>(&tk);
+    const void* vs = raw ? static_cast<const void*>(&iv) : static_cast<const void*>(&tv);
+    const long long ctas = (pl.workers + pl.ops.wpc - 1) / pl.ops.wpc;
+    if (pl.ops.split(ks, vs, p, int(ctas), pl.smem, stream) != cudaSuccess)
         return PKV_ERR_CUDA;
     MqCombine cb;
     cb.part_o = p.part_o; cb.part_ml = p.part_ml; cb.ws_prefix = p.ws_prefix; cb.cu_q = cu_q;

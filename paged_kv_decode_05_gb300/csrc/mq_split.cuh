@@ -81,15 +81,21 @@ struct MqOps {
     int fixed_smem, rt, threads;
     cudaError_t (*prepare)(size_t smem);
     cudaError_t (*occupancy)(int* blocks, size_t smem);
-    // k_src, v_src: CUtensorMap (16-bit caches) or MqI8Src (INT8 caches)
+    // k_src, v_src: CUtensorMap (16-bit caches) or MqI8Src (INT8 caches, and
+    // every cache when `raw`); the int is the number of CTAs
     cudaError_t (*split)(const void* k_src, const void* v_src, const MqParams&, int, size_t,
                          cudaStream_t);
     cudaError_t (*combine)(const MqCombine&, int, cudaStream_t);
+    int wpc;               // workers per CTA
+    bool raw;              // K and V tiles are read through plain pointers (MqI8Src)
 };
 
 // The INT8 split kernels (mq_i8.cu): ops of the variant for this q dtype,
 // head dim, group size and tile height; false if not built.
 bool mq_pick_i8(pkv_dtype q_dtype, int D, int G, int nw, MqOps* o);
+// The short-run split kernel for fp16 / bf16 caches (mq_t.cu): query rows on
+// the MMA's N side in nt tiles of 8 (at most 24 rows); false if not built.
+bool mqt_pick(pkv_dtype kv_dtype, int D, int G, int nt, MqOps* o);
 
 namespace {
 
@@ -874,7 +880,7 @@ struct MqImpl {
         return launch_pdl(mq_combine_kernel<QT, D, G, C::RT>, dim3(grid), dim3(256), 0, st, c);
     }
     static MqOps ops() {
-        return MqOps{C::fixed_bytes(), C::RT, C::NT, prepare, occupancy, split, combine};
+        return MqOps{C::fixed_bytes(), C::RT, C::NT, prepare, occupancy, split, combine, 1, false};
     }
 };
 

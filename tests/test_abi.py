@@ -138,11 +138,15 @@ def test_multiquery_and_copy_blocks_host_validation(lib):
     assert mq(batch=0) == 0
     assert mq(ws_bytes=64) == 3
     assert mq(ws=fake + 128) == 3                # workspace not 256-aligned
-    # size query agrees with the layout: rows per tile 32 (20 rows), one tile
+    # size query agrees with the layout: 20 rows (5 queries x group 4) take
+    # the short-run kernel's tile of 24 rows, one tile per (sequence, kv head)
     dd = desc(nb=64, h=2, d=128)
     slots = 4 * 2 * 1 + 16
     a = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert lib.pkv_multiquery_workspace_size(4, 8, 5, ctypes.byref(dd), 16) == \
+        a(4 * 5) + a(slots * 24 * 2 * 4) + a(slots * 24 * 128 * 4)
+    # 28 rows (7 queries x group 4): the mma.sync kernel's 32-row tile
+    assert lib.pkv_multiquery_workspace_size(4, 8, 7, ctypes.byref(dd), 16) == \
         a(4 * 5) + a(slots * 32 * 2 * 4) + a(slots * 32 * 128 * 4)
     # block copy
     assert lib.pkv_copy_blocks(fake, fake, None, None, ctypes.byref(d), fake, fake, 0, None,

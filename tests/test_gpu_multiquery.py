@@ -55,6 +55,13 @@ SMALL = {
                          kv_dtype="f16", q_dtype="f16", src_dtype="f16", q_len=9,
                          len_groups=((6, 9, 500),)),
     "g4_q1": variant(CONFIGS["gqa8b"], batch=9, len_groups=((9, 1, 700),)),
+    # 7 queries x group 4 = 28 rows: the mma.sync kernel's 32-row tile (fewer
+    # than 25 rows take the short-run kernel, rows on the MMA's N side)
+    "g4_q7": variant(CONFIGS["spec_verify"], batch=7, q_len=7, len_groups=((7, 7, 600),)),
+    "g2_q8_d64": variant(CONFIGS["gqa8b"], batch=6, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                         q_len=8, len_groups=((6, 8, 500),)),
+    "g8_q3_f16": variant(CONFIGS["gqa70b"], batch=5, q_len=3, kv_dtype="f16", q_dtype="f16",
+                         src_dtype="f16", len_groups=((5, 3, 700),)),
     # group 8 (64 q / 8 kv heads)
     "g8_q5": variant(CONFIGS["gqa70b"], batch=8, q_len=5, len_groups=((8, 5, 800),)),
     # INT8 caches (the mma.sync kernel with codes entering as fp16 carriers)
@@ -114,6 +121,26 @@ def test_variable_query_counts_including_empty():
         out = run_mq(g, qv, cu, qmax, parts)
         _sync()
         assert_attention_close(out_to_f64(out), want, False, f"varlen parts={parts}")
+
+
+@pytest.mark.parametrize("parts", [0, 3, 40])
+def test_short_runs_with_variable_query_counts(parts):
+    """Speculative verification with 0..5 queries per sequence (the short-run
+    kernel): every row against the causal oracle."""
+    w, g, o, _ = case("spec_verify")
+    rng = np.random.default_rng(11)
+    qmax = w.cfg.q_len
+    ns = rng.integers(0, qmax + 1, size=w.cfg.batch).astype(np.int32)
+    ns[:3] = (0, 1, qmax)
+    rows = [w.q[b * qmax: b * qmax + int(ns[b])] for b in range(w.cfg.batch)]
+    qv = np.concatenate(rows)
+    cu = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    want = oracle.paged_multiquery_attention(qv, cu, o.k, o.v, w.block_tables, w.context_lens,
+                                             w.cfg.softmax_scale)
+    out = run_mq(g, qv, cu, qmax, parts)
+    _sync()
+    assert int(g.status.item()) == 0
+    assert_attention_close(out_to_f64(out), want, False, f"short varlen parts={parts}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "i8"])
