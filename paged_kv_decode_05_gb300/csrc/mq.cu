@@ -529,6 +529,19 @@ bool encode_cache_map(CUtensorMap* m, const void* base, bool bf16, int D, long l
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// INT8 cache [rows, 128] of byte codes as 16 x 128-byte boxes, 128-byte swizzle.
+bool encode_i8_map(CUtensorMap* m, const void* base, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 16};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // tcgen05 row-tile path: launchers by cache type, head dim and group size.
 using TcLaunch = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const MqParams&, int,
                                  cudaStream_t);
@@ -593,12 +606,12 @@ pkv_status mq_plan(const pkv_cache_desc* c, int batch, int hq, int max_q, pkv_dt
     const long long rows = (long long)max_q * pl->G;
     if (rows > (1LL << 24)) return PKV_ERR_UNSUPPORTED;
     pl->nw = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
-    bool ok;
-    if (c->kv_dtype == PKV_I8)
+    // short runs: rows on the MMA's N side, a warp per worker (INT8: head_dim 128)
+    bool ok = rows <= kMqtMaxRows &&
+              mqt_pick(c->kv_dtype, q_dtype, c->head_dim, pl->G, int((rows + 7) / 8), &pl->ops);
+    if (!ok && c->kv_dtype == PKV_I8)
         ok = mq_pick_i8(q_dtype, c->head_dim, pl->G, pl->nw, &pl->ops);
-    else if (rows <= kMqtMaxRows)   // short runs: rows on the MMA's N side, a warp per worker
-        ok = mqt_pick(c->kv_dtype, c->head_dim, pl->G, int((rows + 7) / 8), &pl->ops);
-    else
+    else if (!ok)
         ok = c->kv_dtype == PKV_BF16 ? mq_pick_d<BF16, BF16>(c->head_dim, pl->G, pl->nw, &pl->ops)
                                      : mq_pick_d<F16, F16>(c->head_dim, pl->G, pl->nw, &pl->ops);
     if (!ok) return PKV_ERR_UNSUPPORTED;
@@ -669,13 +682,20 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     if (!workspace || workspace_bytes < pl.ws_total || !mq_aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
     const long long rows = (long long)cache->num_blocks * cache->num_kv_heads * kBlockSize;
-    // INT8 tiles, and the tiles of the short-run kernel, are read by 1-D bulk
-    // copies instead of tensor maps
+    // 16-bit tiles through tensor maps; INT8 tiles through tensor maps of the
+    // codes (short-run kernel) or 1-D bulk copies (the 32-row kernel)
     CUtensorMap tk = {}, tv = {};
-    if (!i8 && !pl.ops.raw &&
+    if (pl.ops.src == kMqSrcMap &&
         (!encode_cache_map(&tk, k_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows) ||
          !encode_cache_map(&tv, v_cache, cache->kv_dtype == PKV_BF16, cache->head_dim, rows)))
         return PKV_ERR_CUDA;
+    MqI8Map mk = {}, mv = {};
+    if (pl.ops.src == kMqSrcI8Map) {
+        if (!encode_i8_map(&mk.map, k_cache, rows) || !encode_i8_map(&mv.map, v_cache, rows))
+            return PKV_ERR_CUDA;
+        mk.scales = k_scales;
+        mv.scales = v_scales;
+    }
     // Query runs of 16-bit caches that fill 128-row tiles take the tcgen05
     // kernel (no split, no combine, no workspace); shorter runs, and every run
     // over an INT8 cache, the mma.sync kernel below.
@@ -717,9 +737,12 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     p.stall_cta = stall_cta;
     if (pl.ops.prepare(pl.smem) != cudaSuccess) return PKV_ERR_CUDA;
     const MqI8Src ik{k_cache, k_scales}, iv{v_cache, v_scales};
-    const bool raw = i8 || pl.ops.raw;
-    const void* ks = raw ? static_cast<const void*>(&ik) : static_cast<const void*>(&tk);
-    const void* vs = raw ? static_cast<const void*>(&iv) : static_cast<const void*>(&tv);
+    const void* ks = pl.ops.src == kMqSrcRaw ? static_cast<const void*>(&ik)
+                     : pl.ops.src == kMqSrcI8Map ? static_cast<const void*>(&mk)
+                                                 : static_cast<const void*>(&tk);
+    const void* vs = pl.ops.src == kMqSrcRaw ? static_cast<const void*>(&iv)
+                     : pl.ops.src == kMqSrcI8Map ? static_cast<const void*>(&mv)
+                                                 : static_cast<const void*>(&tv);
     const long long ctas = (pl.workers + pl.ops.wpc - 1) / pl.ops.wpc;
     if (pl.ops.split(ks, vs, p, int(ctas), pl.smem, stream) != cudaSuccess)
         return PKV_ERR_CUDA;

@@ -66,6 +66,12 @@ struct MqI8Src {
     const void* cache;
     const float* scales;
 };
+// An INT8 cache read through a 2-D tensor map (128-byte rows of codes, the
+// 128-byte swizzle), with its scales: the short-run INT8 kernel's source.
+struct MqI8Map {
+    CUtensorMap map;
+    const float* scales;
+};
 
 struct MqCombine {
     const float* part_o;
@@ -81,21 +87,24 @@ struct MqOps {
     int fixed_smem, rt, threads;
     cudaError_t (*prepare)(size_t smem);
     cudaError_t (*occupancy)(int* blocks, size_t smem);
-    // k_src, v_src: CUtensorMap (16-bit caches) or MqI8Src (INT8 caches, and
-    // every cache when `raw`); the int is the number of CTAs
+    // k_src, v_src: as `src` says; the int is the number of CTAs
     cudaError_t (*split)(const void* k_src, const void* v_src, const MqParams&, int, size_t,
                          cudaStream_t);
     cudaError_t (*combine)(const MqCombine&, int, cudaStream_t);
     int wpc;               // workers per CTA
-    bool raw;              // K and V tiles are read through plain pointers (MqI8Src)
+    int src;               // kMqSrc*: how the split kernel reads K and V
 };
+constexpr int kMqSrcMap = 0;     // CUtensorMap of a 16-bit cache
+constexpr int kMqSrcRaw = 1;     // MqI8Src: plain pointers (INT8 caches)
+constexpr int kMqSrcI8Map = 2;   // MqI8Map: tensor map of an INT8 cache + its scales
 
 // The INT8 split kernels (mq_i8.cu): ops of the variant for this q dtype,
 // head dim, group size and tile height; false if not built.
 bool mq_pick_i8(pkv_dtype q_dtype, int D, int G, int nw, MqOps* o);
-// The short-run split kernel for fp16 / bf16 caches (mq_t.cu): query rows on
-// the MMA's N side in nt tiles of 8 (at most 24 rows); false if not built.
-bool mqt_pick(pkv_dtype kv_dtype, int D, int G, int nt, MqOps* o);
+// The short-run split kernels (mq_t.cu): query rows on the MMA's N side in nt
+// tiles of 8 (at most 24 rows), for fp16 / bf16 caches (q of the cache type)
+// and for INT8 caches at head_dim 128 (q bf16 or fp16); false if not built.
+bool mqt_pick(pkv_dtype kv_dtype, pkv_dtype q_dtype, int D, int G, int nt, MqOps* o);
 
 namespace {
 
@@ -880,7 +889,8 @@ struct MqImpl {
         return launch_pdl(mq_combine_kernel<QT, D, G, C::RT>, dim3(grid), dim3(256), 0, st, c);
     }
     static MqOps ops() {
-        return MqOps{C::fixed_bytes(), C::RT, C::NT, prepare, occupancy, split, combine, 1, false};
+        return MqOps{C::fixed_bytes(), C::RT, C::NT, prepare, occupancy, split, combine, 1,
+                     Elem<KV>::bytes == 1 ? kMqSrcRaw : kMqSrcMap};
     }
 };
 

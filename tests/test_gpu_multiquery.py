@@ -73,6 +73,11 @@ SMALL = {
                           len_groups=((6, 3, 600),)),
     "int8_g1_q2": variant(CONFIGS["spec_verify_int8"], batch=5, num_q_heads=4, num_kv_heads=4,
                           q_len=2, len_groups=((5, 2, 400),)),
+    # 7 queries x group 4 = 28 rows over an INT8 cache at head_dim 128: the
+    # 32-row kernel (24 rows or fewer take the short-run INT8 kernel)
+    "int8_q7": variant(CONFIGS["spec_verify_int8"], batch=7, q_len=7, len_groups=((7, 7, 600),)),
+    "int8_q3_f16": variant(CONFIGS["spec_verify_int8"], batch=6, q_dtype="f16", src_dtype="f16",
+                           q_len=3, len_groups=((6, 3, 500),)),
 }
 _cache = {}
 
@@ -123,11 +128,12 @@ def test_variable_query_counts_including_empty():
         assert_attention_close(out_to_f64(out), want, False, f"varlen parts={parts}")
 
 
+@pytest.mark.parametrize("name", ["spec_verify", "int8_q5"])
 @pytest.mark.parametrize("parts", [0, 3, 40])
-def test_short_runs_with_variable_query_counts(parts):
+def test_short_runs_with_variable_query_counts(name, parts):
     """Speculative verification with 0..5 queries per sequence (the short-run
-    kernel): every row against the causal oracle."""
-    w, g, o, _ = case("spec_verify")
+    kernels, bf16 and INT8): every row against the causal oracle."""
+    w, g, o, _ = case(name)
     rng = np.random.default_rng(11)
     qmax = w.cfg.q_len
     ns = rng.integers(0, qmax + 1, size=w.cfg.batch).astype(np.int32)
@@ -136,11 +142,12 @@ def test_short_runs_with_variable_query_counts(parts):
     qv = np.concatenate(rows)
     cu = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
     want = oracle.paged_multiquery_attention(qv, cu, o.k, o.v, w.block_tables, w.context_lens,
-                                             w.cfg.softmax_scale)
+                                             w.cfg.softmax_scale, o.ks, o.vs)
     out = run_mq(g, qv, cu, qmax, parts)
     _sync()
     assert int(g.status.item()) == 0
-    assert_attention_close(out_to_f64(out), want, False, f"short varlen parts={parts}")
+    assert_attention_close(out_to_f64(out), want, w.cfg.kv_dtype == "i8",
+                           f"short varlen {name} parts={parts}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "i8"])
