@@ -16,20 +16,21 @@ namespace {
 // tokens in chunks of 64 (four blocks) on the 5th-generation tensor cores:
 //   S = Q K^T      tcgen05.mma kind::f16, M = 128, N = 64, K = D, fp32 in TMEM
 //   softmax        one thread per row reads its S row from TMEM (no shuffles)
-//   O += P V       tcgen05.mma, M = 128, N = D, K = 64; P from shared memory
-//                  (hi + lo 16-bit parts), V read MN-major straight from its
-//                  TMA tile; O stays in TMEM for the whole tile.
+//   O += P V       tcgen05.mma, M = 128, N = D, K = 64; P from tensor memory
+//                  (hi + lo 16-bit parts, written by the softmax over its own
+//                  S buffer), V read MN-major straight from its TMA tile; O
+//                  stays in TMEM for the whole tile.
 // Warp 0 produces (TMA of K/V chunks into NSTG stages), warp 1 issues the MMAs
 // and owns the TMEM allocation, warps 2-9 run the softmax and the epilogue
 // (four warps per tile, one thread per row).
 // Operands in shared memory use the 128-byte swizzle (TMA writes K/V that way;
-// Q and P are written by threads in the same pattern). O is rescaled only when
+// Q is written by threads in the same pattern). O is rescaled only when
 // a row's running maximum grows by more than 2^8 (then exactly); in between P
 // is taken against the older maximum, and O and l always share it.
 
 constexpr int kTcRows = 128;       // rows per tile (TMEM lanes)
 constexpr int kTcChunk = 64;       // tokens per chunk
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 5;
 constexpr float kTcLazy = 8.0f;    // log2 growth of the max tolerated before rescaling O
 
 // Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
@@ -125,6 +126,27 @@ __device__ __forceinline__ void tc_st32(uint32_t addr, const float* v) {
                  : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// 16 consecutive 32-bit columns of this thread's TMEM lane, no wait (the
+// caller waits once with tc_wait_st).
+__device__ __forceinline__ void tc_st16(uint32_t addr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                 "%11,%12,%13,%14,%15,%16};"
+                 :: "r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                    "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+                    "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// d (TMEM) += a (TMEM: M rows in lanes, K 16-bit values packed two per
+// column) * b (shared-memory descriptor).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
 __device__ __forceinline__ void tc_named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
@@ -133,7 +155,12 @@ __device__ __forceinline__ void tc_named_sync(int id, int threads) {
 // one tile's softmax runs, the tensor core works on the other tile's S or
 // P.V. Warps 2-5 are tile 0's softmax, warps 6-9 tile 1's. TMEM (512
 // columns): S buffers of tile x at 128 x + 64 (c % 2), O of tile x at
-// 256 + 128 x.
+// 256 + 128 x. P of chunk c replaces S of chunk c in its buffer (hi in the
+// first 32 columns, lo in the next 32, two 16-bit values per column): the
+// MMAs of a thread run in issue order, so the P.V of chunk c reads it before
+// the S of chunk c + 2 overwrites the buffer, and the softmax of chunk c
+// writes it while the P.V of chunk c - 1 still runs (it waits for that P.V
+// only before touching O).
 constexpr int kTcThreads = 64 + 2 * kTcRows;
 
 template <int D>
@@ -143,11 +170,9 @@ struct TcCfg {
     static constexpr int KV_STAGE = 2 * NH * HALF;
     static constexpr int QHALF = kTcRows * 128;
     static constexpr int QTILE = NH * QHALF;
-    static constexpr int PBYTES = kTcRows * kTcChunk * 2;
     static constexpr int OFF_Q = 0;                                  // tile x at OFF_Q + x QTILE
     static constexpr int OFF_KV = OFF_Q + 2 * QTILE;
-    static constexpr int OFF_P = OFF_KV + kTcStages * KV_STAGE;      // tile x: hi, lo
-    static constexpr int OFF_BAR = OFF_P + 4 * PBYTES;
+    static constexpr int OFF_BAR = OFF_KV + kTcStages * KV_STAGE;
     // kv_full[S], kv_empty[S], s_full[2 tiles][2], p_full[2], o_done[2], drain
     static constexpr int NBAR = 2 * kTcStages + 9;
     static constexpr int OFF_MASK = OFF_BAR + NBAR * 8;
@@ -155,7 +180,7 @@ struct TcCfg {
     static constexpr int BYTES = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_COLS = 512;
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms");
+    static_assert(OFF_KV % 1024 == 0, "swizzle atoms");
 };
 
 template <typename KV, int D, int G>
@@ -302,7 +327,6 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             const uint32_t id_s = tc_idesc(ab, 0, kTcChunk, kTcRows);
             const uint32_t id_o = tc_idesc(ab, 1, D, kTcRows);
             const uint64_t dq0 = tc_desc(smem_addr(smem + C::OFF_Q), 16, 1024);
-            const uint64_t dp0 = tc_desc(smem_addr(smem + C::OFF_P), 16, 1024);
             const uint64_t dk0 = tc_desc(smem_addr(smem + C::OFF_KV), 16, 1024);
             const uint64_t dv0 = tc_desc(smem_addr(smem + C::OFF_KV + C::NH * C::HALF), C::HALF, 1024);
             auto issue_s = [&](int c, int x) {
@@ -319,15 +343,16 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             };
             auto issue_pv = [&](int c, int x) {
                 const uint64_t dv = dv0 + uint64_t((c % kTcStages) * (C::KV_STAGE >> 4));
-                const uint64_t dp = dp0 + uint64_t((x * 2 * C::PBYTES) >> 4);
+                // P of chunk c (hi at columns 0-31, lo at 32-63 of its S buffer)
+                const uint32_t tp = tmem + x * 2 * kTcChunk + (c & 1) * kTcChunk;
                 const uint32_t to = tmem + 4 * kTcChunk + x * 128;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kTcChunk / 16; ++kk)
-                        tc_mma(to, dp + uint64_t((part * C::PBYTES + kk * 32) >> 4),
-                               dv + uint64_t((kk * 16 * 128) >> 4), id_o,
-                               (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_ts(to, tp + part * (kTcChunk / 2) + kk * 8,
+                                  dv + uint64_t((kk * 16 * 128) >> 4), id_o,
+                                  (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(smem_addr(&o_done[x]));
             };
             auto finish = [&](int c) -> bool {   // P.V of chunk c for both tiles
@@ -367,7 +392,6 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             const bool rv = qi < n;
             const int pos = L - n + qi;
             float m = -INFINITY, l = 0.f;
-            unsigned char* ph = smem + C::OFF_P + x * 2 * C::PBYTES + r * 128;
             const int last_blk_tok = ((L - 1) / kBlockSize) * kBlockSize;
             const bool qpos = p.qscale > 0.f;                  // max of raw scores = max of scaled
             bool ok = true;
@@ -400,41 +424,32 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                             mx = fmaxf(mx, s[i]);
                         }
                     }
-                    if (c > 0) ok = __all_sync(kFull, wait(&o_done[x], (c - 1) & 1, 0x1000u));
                 }
                 if (ok) {
-                    tc_fence_after();
                     const bool grow = mx > m + kTcLazy || (m == -INFINITY && mx > -INFINITY);
-                    if (c > 0 && __any_sync(kFull, grow && m > -INFINITY)) {
-                        const float a = (grow && m > -INFINITY) ? fast_exp2(m - mx) : 1.f;
-#pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            float o[32];
-                            tc_ld32(tm_o + lane_addr + c0, o);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= a;
-                            tc_st32(tm_o + lane_addr + c0, o);
-                        }
-                        if (grow && m > -INFINITY) l *= a;
-                    }
+                    const bool rescale = c > 0 && __any_sync(kFull, grow && m > -INFINITY);
+                    const float a = (grow && m > -INFINITY) ? fast_exp2(m - mx) : 1.f;
+                    if (grow && m > -INFINITY) l *= a;
                     if (grow) m = mx;
-                    // P = exp2(s - m) as hi + lo 16-bit parts, written swizzled (row r)
+                    // P = exp2(s - m) as hi + lo 16-bit parts, packed two per
+                    // column into this chunk's S buffer (its own TMEM lane), where
+                    // the P.V MMAs take it as their A operand
+                    const uint32_t tp = tm_s + lane_addr + (c & 1) * kTcChunk;
                     auto emit = [&](auto expo) {
 #pragma unroll
-                        for (int c16 = 0; c16 < kTcChunk / 8; ++c16) {
-                            uint32_t hw[4], lw[4];
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t hw[16], lw[16];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float x0 = expo(s[c16 * 8 + 2 * e]);
-                                const float x1 = expo(s[c16 * 8 + 2 * e + 1]);
+                            for (int e = 0; e < 16; ++e) {
+                                const float x0 = expo(s[32 * h + 2 * e]);
+                                const float x1 = expo(s[32 * h + 2 * e + 1]);
                                 l += x0 + x1;
                                 hw[e] = pack2<KV>(x0, x1);
                                 const float2 rr = unpack2(KV{}, hw[e]);
                                 lw[e] = pack2<KV>(x0 - rr.x, x1 - rr.y);
                             }
-                            const uint32_t off = uint32_t((c16 ^ (r & 7)) << 4);
-                            *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                            *reinterpret_cast<uint4*>(ph + C::PBYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                            tc_st16(tp + 16 * h, hw);
+                            tc_st16(tp + kTcChunk / 2 + 16 * h, lw);
                         }
                     };
                     if (plain) {   // finite raw scores, m finite: one fma and one ex2 each
@@ -443,9 +458,23 @@ mq_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                     } else {
                         emit([&](float y) { return y == -INFINITY ? 0.f : fast_exp2(y - m); });
                     }
+                    tc_wait_st();
+                    // O may be touched only once the previous chunk's P.V is done
+                    if (c > 0) ok = __all_sync(kFull, wait(&o_done[x], (c - 1) & 1, 0x1000u));
+                    if (ok && rescale) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            float o[32];
+                            tc_ld32(tm_o + lane_addr + c0, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= a;
+                            tc_st32(tm_o + lane_addr + c0, o);
+                        }
+                    }
                     // tile 0 zeroes V rows past the context (both tiles' P.V
                     // follow tile 0's P in the MMA thread's order)
-                    if (x == 0 && last_blk_tok >= tok0 && last_blk_tok < tok0 + kTcChunk &&
+                    if (ok && x == 0 && last_blk_tok >= tok0 && last_blk_tok < tok0 + kTcChunk &&
                         L < last_blk_tok + kBlockSize) {
                         const int jj = (last_blk_tok - tok0) / kBlockSize;
                         if ((mask >> jj) & 1) {
