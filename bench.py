@@ -769,16 +769,18 @@ def run_multiquery(args):
     tflops = flops / (attn_ms / 1e3) / 1e12
     # The library's dispatch rule: runs over fp16 / bf16 caches that fill
     # 128-row tiles (q_len x the group size) take the tcgen05 kernel, one
-    # launch; runs of at most 24 rows over fp16 / bf16 caches the short-run
-    # split kernel and the combine, other runs and INT8 caches the mma.sync
-    # split kernel and the combine, two launches each. Plus the append (two
-    # kernels for INT8).
+    # launch; runs of at most 24 rows take a short-run split kernel (fp16 /
+    # bf16 caches, and INT8 caches at head_dim 128) and the combine, other
+    # runs the 16-rows-per-warp split kernel and the combine, two launches
+    # each. Plus the append (two kernels for INT8).
     g = cfg.num_q_heads // cfg.num_kv_heads
     rows = nq * g
-    if cfg.kv_dtype != "i8" and rows >= 128:
+    i8 = cfg.kv_dtype == "i8"
+    if not i8 and rows >= 128:
         kernel, src = "mq_tc_kernel", ("mq_split.cuh", "mq.cu")
-    elif cfg.kv_dtype != "i8" and rows <= 24:
-        kernel, src = "mqt_split_kernel", ("mq_split.cuh", "mq_t.cu")
+    elif rows <= 24 and (not i8 or cfg.head_dim == 128):
+        kernel = "mqt_i8_split_kernel" if i8 else "mqt_split_kernel"
+        src = ("mq_split.cuh", "mq_t.cu")
     else:
         kernel, src = "mq_split_kernel", ("mq_split.cuh",)
     tc = kernel == "mq_tc_kernel"

@@ -284,11 +284,11 @@ pkv_status pkv_merge_states(const float *part_m, const float *part_l, const floa
  *    aligned: a tcgen05 / tensor-memory kernel with one CTA per (sequence,
  *    kv head, 128-row tile) and no split (num_parts and the workspace are
  *    then not used, but are still checked);
- *  - fp16 / bf16 caches, rows <= 24 (speculative verification): an mma.sync
- *    kernel with the rows on the MMA's N side, one warp per worker
- *    (num_parts counts warps);
- *  - otherwise, and for every INT8 cache: an mma.sync kernel with 16 rows
- *    per warp, one CTA per worker.
+ *  - rows <= 24 (speculative verification) over fp16 / bf16 caches, or over
+ *    INT8 caches at head_dim 128: an mma.sync kernel with the rows on the
+ *    MMA's N side, one warp per worker (num_parts counts warps);
+ *  - otherwise: an mma.sync kernel with 16 rows per warp, one CTA per
+ *    worker.
  * The split kernels cut their stream of units into num_parts ranges and a
  * combine kernel merges the pieces through the workspace. All compute the
  * same causal attention within the same tolerance (INT8: within 2e-2 of
