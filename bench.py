@@ -2,11 +2,12 @@
 
 A step is the whole hot path for one batch: write the step's new K/V token
 per sequence into the paged cache, then paged decode attention with its
-split-K combine. For fp16/bf16 caches the write is folded into the split
-kernel (pkv_decode_step + pkv_decode_combine, 2 launches; --unfused runs
-pkv_append + pkv_decode_split + pkv_decode_combine); INT8 caches run
-pkv_append + split + combine. Default workload: the GQA Llama-3-8B-shape
-batch (B=256, 32 q / 8 kv heads, D=128, bf16, L~U[128,4096]).
+split-K combine, through pkv_decode_step + pkv_decode_combine: for fp16/bf16
+caches the write is folded into the split kernel (2 launches), for INT8
+caches one append kernel writes the rows (3 launches). --unfused runs
+pkv_append + pkv_decode_split + pkv_decode_combine (3 launches; INT8: 4).
+Default workload: the GQA Llama-3-8B-shape batch (B=256, 32 q / 8 kv heads,
+D=128, bf16, L~U[128,4096]).
 
     python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
 
@@ -72,8 +73,9 @@ def parse_args(argv=None):
                          "attention (use --config spec_verify or prefill_chunk)")
     ap.add_argument("--copy-pairs", type=int, default=4096)
     ap.add_argument("--unfused", action="store_true",
-                    help="step = pkv_append + split + combine (3 launches) instead of the "
-                         "fused pkv_decode_step (split with the append folded in + combine)")
+                    help="step = pkv_append + split + combine (3 launches; INT8: 4) instead of "
+                         "pkv_decode_step (16-bit: split with the append folded in; INT8: the "
+                         "step's append kernel + split) + combine")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step from a captured CUDA graph instead of eager launches")
     ap.add_argument("--num-parts", type=int, default=0, help="worker warps (0 = device default)")
@@ -373,9 +375,10 @@ def kernel_pass(step, n: int, device, names=("append", "split", "combine")) -> d
 def _step(st, cfg, ws, parts, ev=None, fused=None):
     """One decode step: the new token's cache write, split, combine.
 
-    Unfused: pkv_append, pkv_decode_split, pkv_decode_combine (3 launches; 6
-    for INT8). Fused (16-bit caches): pkv_decode_step's split phase writes the
-    new rows itself, then pkv_decode_combine (2 launches).
+    Unfused: pkv_append, pkv_decode_split, pkv_decode_combine (3 launches; 4
+    for INT8). Fused: pkv_decode_step's split phase (16-bit caches: the split
+    kernel writes the new rows itself; INT8: the step's append kernel, then
+    the split), then pkv_decode_combine (2 launches; 3 for INT8).
     ``ev``: optional 4 CUDA events recorded before the append, before the
     split, before the combine and after it (the first two coincide if fused).
     """
@@ -393,7 +396,8 @@ def _step(st, cfg, ws, parts, ev=None, fused=None):
     if fused:
         B.pkv_decode_step(st["q"], st["k_step"], st["v_step"], st["k_cache"], st["v_cache"],
                           st["block_tables"], st["context_lens"], cfg.softmax_scale, st["out"],
-                          ws, parts, st["status"], run_combine=False)
+                          ws, parts, st["status"], run_combine=False, k_scales=st["k_scales"],
+                          v_scales=st["v_scales"])
     else:
         B.pkv_decode_split(st["q"], st["k_cache"], st["v_cache"], st["block_tables"],
                            st["context_lens"], cfg.softmax_scale, st["out"], ws,
@@ -428,8 +432,8 @@ def run_native(args):
     ws = torch.empty(B.pkv_decode_workspace_size(cfg.batch, cfg.num_q_heads, st["k_cache"], parts),
                      dtype=torch.uint8, device=device)
     alg = algorithmic_bytes(cfg, w.context_lens)
-    st["fused"] = (not args.unfused) and cfg.kv_dtype != "i8"
-    launches_per_step = 2 if st["fused"] else (4 if cfg.kv_dtype == "i8" else 3)
+    st["fused"] = not args.unfused
+    launches_per_step = (2 if st["fused"] else 3) + (1 if cfg.kv_dtype == "i8" else 0)
     K, W = args.steps, args.warmup
 
     props = torch.cuda.get_device_properties(device)
@@ -475,7 +479,14 @@ def run_native(args):
     n_kp = args.kernel_steps or int(min(KERNEL_PASS_MAX_STEPS,
                                         max(KERNEL_PASS_MIN_STEPS,
                                             KERNEL_PASS_MIN_MS * K / max(ms_total, 1e-6))))
-    kp = kernel_pass(lambda ev: _step(st, cfg, ws, parts, ev), n_kp, device)
+    # INT8: pkv_decode_step runs its append kernel and the split in one call,
+    # so this pass times the steps through pkv_append + split + combine (the
+    # same split and combine kernels; pkv_append writes the same codes and
+    # scales as the step's append kernel, so the cache state is unchanged)
+    kp_fused = st["fused"] and cfg.kv_dtype != "i8"
+    kp = kernel_pass(lambda ev: _step(st, cfg, ws, parts, ev, fused=kp_fused), n_kp, device)
+    if st["fused"] and not kp_fused:
+        kp["append_timed_as"] = "pkv_append (two kernels) in place of the step's append kernel"
     wall2 = time.time()
 
     # ---- end-to-end through the C ABI with host buffers (H2D inputs, D2H output)
@@ -497,8 +508,10 @@ def run_native(args):
                    "l2": "no flush: the KV cache read each step (%.2f GB) is far larger than "
                          "the 129 MB L2" % (alg / 1e9),
                    "parallelism": f"replicas x{world}",
-                   "step": ("pkv_decode_step split phase (new K/V rows written by the split "
-                            "kernel) + pkv_decode_combine" if st["fused"] else
+                   "step": (("pkv_decode_step split phase (the step's INT8 append kernel, "
+                             "then the split) + pkv_decode_combine" if cfg.kv_dtype == "i8" else
+                             "pkv_decode_step split phase (new K/V rows written by the split "
+                             "kernel) + pkv_decode_combine") if st["fused"] else
                             "pkv_append + pkv_decode_split + pkv_decode_combine")},
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peak, 2),
@@ -514,6 +527,8 @@ def run_native(args):
         "kernel_ms": {**{k: {kk: round(vv, 6) for kk, vv in v.items()}
                          for k, v in kp.items() if isinstance(v, dict)},
                       "steps": kp["steps"], "skipped": kp["skipped"],
+                      **({"append_timed_as": kp["append_timed_as"]}
+                         if "append_timed_as" in kp else {}),
                       "how": "separate pass after the timed region: CUDA events around each "
                              "kernel of every step (the first steps dropped), median"},
         "launch_mode": "cuda_graph" if graph is not None else "eager",

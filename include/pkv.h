@@ -188,22 +188,28 @@ pkv_status pkv_decode_split(const void *q, pkv_dtype q_dtype,
                             void *workspace, size_t workspace_bytes, int32_t num_parts,
                             uint32_t *dev_status, cudaStream_t stream);
 
-/* The decode step's cache write and attention in one call (fp16 / bf16
- * caches): writes k_new[b], v_new[b] ([batch, num_kv_heads, head_dim], cache
- * dtype) at position context_lens[b] - 1 of each sequence, i.e. physical
- * block block_tables[b, (L-1)/16], row (L-1)%16 (nothing for L == 0), then
- * computes pkv_decode_attn over the caches including that token. The same
- * result as pkv_append with those slots followed by pkv_decode_attn, one
- * launch fewer: the split kernel copies each new row into shared memory in
- * place of the tile's row (from k_new / v_new, beside the cache rows before
- * it) and stores it into the cache from there. The block receiving a
+/* The decode step's cache write and attention in one call: writes k_new[b],
+ * v_new[b] ([batch, num_kv_heads, head_dim]; the cache dtype for fp16 / bf16
+ * caches, q_dtype for INT8 caches) at position context_lens[b] - 1 of each
+ * sequence, i.e. physical block block_tables[b, (L-1)/16], row (L-1)%16
+ * (nothing for L == 0), then computes pkv_decode_attn over the caches
+ * including that token. The same result, bit for bit in the cache (codes
+ * and scales for INT8) and in out, as pkv_append with those slots followed
+ * by pkv_decode_attn, in fewer launches: for fp16 / bf16 caches the split
+ * kernel copies each new row into shared memory in place of the tile's row
+ * (from k_new / v_new, beside the cache rows before it) and stores it into
+ * the cache from there (split [+ combine]); for INT8 caches one append
+ * kernel settles each touched tile's scales, requantises it if a scale
+ * grows and encodes the row, one warp per (sequence, kv head), without
+ * pkv_append's gather pass (append + split [+ combine]; k_scales, v_scales
+ * as for pkv_append, NULL for 16-bit caches). The block receiving a
  * sequence's new token must not be shared with another sequence
  * (copy-on-write). Same workspace as pkv_decode_attn; k_new, v_new 16-byte
- * aligned. run_combine = 0 runs only the
- * split phase (as pkv_decode_split; pkv_decode_combine must follow), 1 both.
- * INT8 caches: use pkv_append + pkv_decode_attn (PKV_ERR_UNSUPPORTED here). */
+ * aligned. run_combine = 0 runs only the split phase (as pkv_decode_split;
+ * pkv_decode_combine must follow), 1 both. */
 pkv_status pkv_decode_step(const void *q, pkv_dtype q_dtype, const void *k_new,
                            const void *v_new, void *k_cache, void *v_cache,
+                           float *k_scales, float *v_scales,
                            const pkv_cache_desc *cache, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t batch, int32_t num_q_heads, float softmax_scale, void *out,

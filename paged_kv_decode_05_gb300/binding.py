@@ -51,9 +51,9 @@ _SIGS = {
     "pkv_decode_split": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
                                         _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _P, _P]),
     "pkv_decode_combine": (ctypes.c_int, [_DESC, _I32, _I32, ctypes.c_int, _P, _P, _SZ, _I32, _P]),
-    "pkv_decode_step": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _DESC, _P, _I32, _P,
-                                       _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _I32, _P,
-                                       _P]),
+    "pkv_decode_step": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _DESC, _P, _I32,
+                                       _P, _I32, _I32, ctypes.c_float, _P, _P, _SZ, _I32, _I32,
+                                       _P, _P]),
     "pkv_copy_blocks": (ctypes.c_int, [_P, _P, _P, _P, _DESC, _P, _P, _I32, _P, _P]),
     "pkv_multiquery_workspace_size": (_SZ, [_I32, _I32, _I32, _DESC, _I32]),
     "pkv_multiquery_attn": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _P, _P, _DESC, _P,
@@ -192,13 +192,16 @@ def pkv_decode_split(q, k_cache, v_cache, block_tables, context_lens, softmax_sc
 
 
 def pkv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, softmax_scale,
-                    out, workspace, num_parts=0, dev_status=None, stream=None, run_combine=True):
+                    out, workspace, num_parts=0, dev_status=None, stream=None, run_combine=True,
+                    k_scales=None, v_scales=None):
     """Write ``k_new/v_new [B, Hkv, D]`` at each sequence's last position, then attend
-    (``run_combine=False``: split phase only; :func:`pkv_decode_combine` must follow)."""
+    (``run_combine=False``: split phase only; :func:`pkv_decode_combine` must follow).
+    INT8 caches take their ``k_scales/v_scales``."""
     desc = cache_desc(k_cache)
     B, Hq, D = q.shape
     code = lib().pkv_decode_step(
         _ptr(q), _dtype_code(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scales), _ptr(v_scales),
         ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
         B, Hq, float(softmax_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), int(num_parts), int(bool(run_combine)),

@@ -234,6 +234,71 @@ __global__ void __launch_bounds__(kThreads, 4) i8_settle_kernel(I8Args a) {
     }
 }
 
+// The decode step's append over an INT8 cache: one new token per sequence,
+// at position L_b - 1, so each (block, kv head) tile receives exactly one
+// row and its warp needs no gather pass: the same settle, requantisation and
+// encoding as i8_settle_kernel, for the one row (codes and scales come out
+// bit for bit as pkv_append's for the same slots). One warp per (sequence,
+// kv head); sequences with L = 0, an over-long length or an out-of-pool
+// table entry write nothing (the split kernel flags them).
+struct I8StepArgs {
+    const void* k_new;            // [batch, hkv, D]
+    const void* v_new;
+    int8_t* k_cache;
+    int8_t* v_cache;
+    float* k_scales;
+    float* v_scales;
+    const int32_t* block_tables;  // [batch, mb]
+    const int32_t* context_lens;
+    uint32_t* status;
+    int batch, hkv, mb, num_blocks;
+};
+
+template <typename S, int D>
+__global__ void __launch_bounds__(kThreads, 4) i8_step_append_kernel(I8StepArgs a) {
+    griddep_wait();
+    griddep_launch_dependents();
+    constexpr int EPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long items = (long long)a.batch * a.hkv;
+    for (long long it = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; it < items;
+         it += ((long long)gridDim.x * blockDim.x) >> 5) {
+        const int b = int(it / a.hkv), kvh = int(it - (long long)b * a.hkv);
+        // the new rows are loaded while the slot is resolved
+        float xk[EPL], xv[EPL];
+        load_row<S, D>(a.k_new, it * D, xk);
+        load_row<S, D>(a.v_new, it * D, xv);
+        const int L = a.context_lens[b];
+        if (L <= 0 || L > a.mb * kBlockSize) continue;
+        const int blk = a.block_tables[(long long)b * a.mb + (L - 1) / kBlockSize];
+        if (unsigned(blk) >= unsigned(a.num_blocks)) continue;
+        const long long t = (long long)blk * a.hkv + kvh;
+        const int r = (L - 1) % kBlockSize;
+        const float so_k = a.k_scales[t], so_v = a.v_scales[t];
+        float mk = 0.f, mv = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            mk = fmaxf(mk, fabsf(xk[e]));
+            mv = fmaxf(mv, fabsf(xv[e]));
+        }
+        mk = warp_max(mk);
+        mv = warp_max(mv);
+        bool grow_k, grow_v;
+        const float sk = settle_scale(__float_as_uint(mk), so_k, &grow_k);
+        const float sv = settle_scale(__float_as_uint(mv), so_v, &grow_v);
+        if (grow_k) requant_tile<D>(a.k_cache + t * kBlockSize * D, so_k, sk, lane);
+        if (grow_v) requant_tile<D>(a.v_cache + t * kBlockSize * D, so_v, sv, lane);
+        __syncwarp();
+        const long long dst = (t * kBlockSize + r) * D + lane * EPL;
+        store_codes<EPL>(a.k_cache, dst, xk, sk);
+        store_codes<EPL>(a.v_cache, dst, xv, sv);
+        if (lane == 0) {
+            a.k_scales[t] = sk;
+            a.v_scales[t] = sv;
+        }
+    }
+}
+
 int grid_for(long long work_items, int per_block, int cap) {
     long long g = (work_items + per_block - 1) / per_block;
     if (g < 1) g = 1;
@@ -260,7 +325,33 @@ void launch_i8(const I8Args& a, cudaStream_t st) {
     launch_pdl(i8_settle_kernel<S, D>, dim3(g), dim3(kThreads), 0, st, a);
 }
 
+template <typename S, int D>
+cudaError_t launch_i8_step(const I8StepArgs& a, cudaStream_t st) {
+    const long long items = (long long)a.batch * a.hkv;
+    return launch_pdl(i8_step_append_kernel<S, D>, dim3(grid_for(items, kWarps, 1 << 16)),
+                      dim3(kThreads), 0, st, a);
+}
+
 }  // namespace
+
+// The INT8 decode step's append (see i8_step_append_kernel); the caller has
+// checked the arguments.
+cudaError_t launch_i8_step_append(const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                                  void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                  const int32_t* block_tables, int mb, const int32_t* context_lens,
+                                  int batch, int hkv, int D, int num_blocks, uint32_t* status,
+                                  cudaStream_t stream) {
+    I8StepArgs a;
+    a.k_new = k_new; a.v_new = v_new;
+    a.k_cache = static_cast<int8_t*>(k_cache); a.v_cache = static_cast<int8_t*>(v_cache);
+    a.k_scales = k_scales; a.v_scales = v_scales;
+    a.block_tables = block_tables; a.context_lens = context_lens; a.status = status;
+    a.batch = batch; a.hkv = hkv; a.mb = mb; a.num_blocks = num_blocks;
+    if (src_dtype == PKV_BF16)
+        return D == 128 ? launch_i8_step<BF16, 128>(a, stream) : launch_i8_step<BF16, 64>(a, stream);
+    return D == 128 ? launch_i8_step<F16, 128>(a, stream) : launch_i8_step<F16, 64>(a, stream);
+}
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -1178,7 +1178,7 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
                       size_t workspace_bytes, int32_t num_parts, uint32_t* dev_status,
                       cudaStream_t stream, const void* k_new = nullptr,
                       const void* v_new = nullptr, uint64_t wait_ns = kWaitLimitNs,
-                      int stall_worker = -1) {
+                      int stall_worker = -1, bool check_only = false) {
     Ops ops;
     int G = 0;
     pkv_status s = check_decode(cache, batch, hq, q_dtype, &ops, &G);
@@ -1186,7 +1186,7 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
     if (batch == 0) return PKV_OK;
     if (num_parts < 0) return PKV_ERR_INVALID_ARG;
     if (!out || !is_aligned(out, 16)) return PKV_ERR_INVALID_ARG;
-    if (do_split) {
+    if (do_split || check_only) {
         if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
         if (!is_aligned(q, 16) || !is_aligned(k_cache, 16) || !is_aligned(v_cache, 16) ||
             !is_aligned(block_tables, 4) || !is_aligned(context_lens, 4))
@@ -1205,6 +1205,7 @@ pkv_status run_decode(bool do_split, bool do_combine, const void* q, pkv_dtype q
     const Layout l = layout(batch, hkv, G, D, workers);
     if (!workspace || workspace_bytes < l.total || !is_aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
+    if (check_only) return PKV_OK;
     char* ws = static_cast<char*>(workspace);
     if (do_split) {
         const size_t smem = split_smem(ops, batch);
@@ -1304,8 +1305,17 @@ extern "C" pkv_status pkv_decode_split(const void* q, pkv_dtype q_dtype, const v
                       softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream);
 }
 
+namespace pkv {
+cudaError_t launch_i8_step_append(const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                                  void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                  const int32_t* block_tables, int mb, const int32_t* context_lens,
+                                  int batch, int hkv, int D, int num_blocks, uint32_t* status,
+                                  cudaStream_t stream);
+}
+
 extern "C" pkv_status pkv_decode_step(const void* q, pkv_dtype q_dtype, const void* k_new,
                                       const void* v_new, void* k_cache, void* v_cache,
+                                      float* k_scales, float* v_scales,
                                       const pkv_cache_desc* cache, const int32_t* block_tables,
                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
                                       int32_t batch, int32_t num_q_heads, float softmax_scale,
@@ -1313,14 +1323,29 @@ extern "C" pkv_status pkv_decode_step(const void* q, pkv_dtype q_dtype, const vo
                                       int32_t num_parts, int32_t run_combine,
                                       uint32_t* dev_status, cudaStream_t stream) {
     if (!cache) return PKV_ERR_INVALID_ARG;
-    if (cache->kv_dtype == PKV_I8) return PKV_ERR_UNSUPPORTED;
     if (run_combine != 0 && run_combine != 1) return PKV_ERR_INVALID_ARG;
     if (batch > 0 && (!k_new || !v_new || !is_aligned(k_new, 16) || !is_aligned(v_new, 16)))
         return PKV_ERR_INVALID_ARG;
-    return run_decode(true, run_combine == 1, q, q_dtype, k_cache, v_cache, nullptr, nullptr, cache,
-                      block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
-                      softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream,
-                      k_new, v_new);
+    if (cache->kv_dtype != PKV_I8)
+        return run_decode(true, run_combine == 1, q, q_dtype, k_cache, v_cache, nullptr, nullptr,
+                          cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                          num_q_heads, softmax_scale, out, workspace, workspace_bytes, num_parts,
+                          dev_status, stream, k_new, v_new);
+    // INT8: the step's append kernel (one row per tile), then split [+ combine];
+    // every argument is checked (a call that launches nothing) before the append
+    pkv_status s = run_decode(true, run_combine == 1, q, q_dtype, k_cache, v_cache, k_scales,
+                              v_scales, cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                              num_q_heads, softmax_scale, out, workspace, workspace_bytes, num_parts,
+                              dev_status, stream, nullptr, nullptr, kWaitLimitNs, -1, true);
+    if (s != PKV_OK || batch == 0) return s;
+    if (launch_i8_step_append(k_new, v_new, q_dtype, k_cache, v_cache, k_scales, v_scales,
+                              block_tables, max_blocks_per_seq, context_lens, batch,
+                              cache->num_kv_heads, cache->head_dim, cache->num_blocks, dev_status,
+                              stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return run_decode(true, run_combine == 1, q, q_dtype, k_cache, v_cache, k_scales, v_scales,
+                      cache, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                      softmax_scale, out, workspace, workspace_bytes, num_parts, dev_status, stream);
 }
 
 extern "C" pkv_status pkv_decode_combine(const pkv_cache_desc* cache, int32_t batch,

@@ -90,10 +90,12 @@ int main(void) {
                            0.125f, fake, fake, 1u << 30, 64, NULL, NULL) == PKV_ERR_INVALID_ARG);
     CHECK(pkv_decode_combine(&bf16, 4, 32, PKV_BF16, fake, fake, 16, 64, NULL) ==
           PKV_ERR_WORKSPACE);
-    CHECK(pkv_decode_step(fake, PKV_BF16, fake, fake, fake, fake, &i8, fake, 4, fake, 4, 32,
-                          0.125f, fake, fake, 1u << 30, 64, 1, NULL, NULL) == PKV_ERR_UNSUPPORTED);
-    CHECK(pkv_decode_step(fake, PKV_BF16, fake8, fake, fake, fake, &bf16, fake, 4, fake, 4, 32,
-                          0.125f, fake, fake, 1u << 30, 64, 1, NULL, NULL) == PKV_ERR_INVALID_ARG);
+    CHECK(pkv_decode_step(fake, PKV_BF16, fake, fake, fake, fake, NULL, NULL, &i8, fake, 4, fake,
+                          4, 32, 0.125f, fake, fake, 1u << 30, 64, 1, NULL, NULL) ==
+          PKV_ERR_INVALID_ARG);   /* INT8 caches need their scales */
+    CHECK(pkv_decode_step(fake, PKV_BF16, fake8, fake, fake, fake, NULL, NULL, &bf16, fake, 4, fake,
+                          4, 32, 0.125f, fake, fake, 1u << 30, 64, 1, NULL, NULL) ==
+          PKV_ERR_INVALID_ARG);
     CHECK(pkv_decode_attn_noalloc(fake, PKV_BF16, fake, fake, NULL, NULL, &d96, fake, 4, fake, 4,
                                   32, 0.125f, fake, 64, NULL, NULL) == PKV_ERR_UNSUPPORTED);
     CHECK(pkv_decode_attn_noalloc(fake, PKV_BF16, fake, fake, NULL, NULL, &bf16, fake, 4, fake,

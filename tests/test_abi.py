@@ -163,15 +163,16 @@ def test_decode_step_host_validation(lib):
     fake = 0x100000
     d = desc()
 
-    def step(dd=None, k_new=fake, run_combine=1, batch=4, hq=8):
-        return lib.pkv_decode_step(fake, B.PKV_BF16, k_new, fake, fake, fake,
+    def step(dd=None, k_new=fake, run_combine=1, batch=4, hq=8, scales=None):
+        return lib.pkv_decode_step(fake, B.PKV_BF16, k_new, fake, fake, fake, scales, scales,
                                    ctypes.byref(dd or d), fake, 4, fake, batch, hq, 0.125, fake,
                                    fake, 1 << 30, 64, run_combine, None, None)
-    assert step(dd=desc(dt=B.PKV_I8)) == 2       # INT8 caches: append + attend instead
+    assert step(dd=desc(dt=B.PKV_I8)) == 1       # INT8 caches need their scales
+    assert step(dd=desc(dt=B.PKV_I8), scales=fake + 2) == 1   # misaligned scales
     assert step(run_combine=2) == 1
     assert step(k_new=None) == 1
     assert step(k_new=fake + 8) == 1             # the new rows are bulk-copied: 16-byte aligned
     assert step(hq=7) == 1
     assert step(batch=0) == 0
-    assert lib.pkv_decode_step(fake, B.PKV_BF16, fake, fake, fake, fake, None, fake, 4, fake, 4, 8,
-                               0.125, fake, fake, 1 << 30, 64, 1, None, None) == 1
+    assert lib.pkv_decode_step(fake, B.PKV_BF16, fake, fake, fake, fake, None, None, None, fake, 4,
+                               fake, 4, 8, 0.125, fake, fake, 1 << 30, 64, 1, None, None) == 1
