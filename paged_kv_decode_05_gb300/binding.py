@@ -242,7 +242,8 @@ def pkv_multiquery_attn(q, cu_q, max_q_len, k_cache, v_cache, block_tables, cont
     desc = cache_desc(k_cache)
     code = lib().pkv_multiquery_attn(
         _ptr(q), _dtype_code(q), _ptr(cu_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
-        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(context_lens),
         int(cu_q.numel() - 1), int(q.shape[1]), float(softmax_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), int(num_parts), _ptr(dev_status),
         _stream(stream))
@@ -304,7 +305,8 @@ def pkv_testing_multiquery_attn_stall(q, cu_q, max_q_len, k_cache, v_cache, bloc
     desc = cache_desc(k_cache)
     code = lib().pkv_testing_multiquery_attn_stall(
         _ptr(q), _dtype_code(q), _ptr(cu_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
-        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+        _ptr(k_scales), _ptr(v_scales), ctypes.byref(desc), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(context_lens),
         int(cu_q.numel() - 1), int(q.shape[1]), float(softmax_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), int(num_parts), int(wait_limit_ns),
         int(stall_cta), _ptr(dev_status), _stream(stream))

@@ -92,8 +92,11 @@ def test_decode_stall_hook_rejects_bad_arguments():
 
 
 MQ = {
-    # 5 queries x group 4 = 20 rows: the mma.sync split kernel
+    # 5 queries x group 4 = 20 rows: the short-run split kernels (bf16, INT8)
     "spec_verify": variant(CONFIGS["spec_verify"], batch=6, len_groups=((6, 5, 600),)),
+    "spec_verify_int8": variant(CONFIGS["spec_verify_int8"], batch=6, len_groups=((6, 5, 600),)),
+    # 7 queries x group 4 = 28 rows: the 16-rows-per-warp split kernel
+    "rows28": variant(CONFIGS["spec_verify"], batch=6, q_len=7, len_groups=((6, 7, 600),)),
     # 64 queries x group 4 = 256 rows: the tcgen05 kernel
     "prefill_chunk": variant(CONFIGS["prefill_chunk"], batch=2, q_len=64, max_len=500,
                              len_groups=((2, 64, 500),)),
@@ -116,7 +119,7 @@ def test_multiquery_wait_that_runs_out(name):
     t0 = time.time()
     B.pkv_testing_multiquery_attn_stall(q, cu, nq, g.k_cache, g.v_cache, g.block_tables,
                                         g.context_lens, cfg.softmax_scale, out, ws, LIMIT_NS, 0,
-                                        5, status)
+                                        5, status, k_scales=g.k_scales, v_scales=g.v_scales)
     torch.cuda.synchronize()
     elapsed = time.time() - t0
     st = int(status.item())
@@ -124,9 +127,10 @@ def test_multiquery_wait_that_runs_out(name):
     assert elapsed < 3.0, elapsed
     # a normal call on the same context matches the oracle
     B.pkv_multiquery_attn(q, cu, nq, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
-                          cfg.softmax_scale, out, ws, 5, g.status)
+                          cfg.softmax_scale, out, ws, 5, g.status, k_scales=g.k_scales,
+                          v_scales=g.v_scales)
     torch.cuda.synchronize()
     assert int(g.status.item()) == 0
     want = oracle.paged_multiquery_attention(w.q, w.cu_q, o.k, o.v, w.block_tables,
-                                             w.context_lens, cfg.softmax_scale)
-    assert_attention_close(out_to_f64(out), want, False, f"{name} after a stall")
+                                             w.context_lens, cfg.softmax_scale, o.ks, o.vs)
+    assert_attention_close(out_to_f64(out), want, cfg.kv_dtype == "i8", f"{name} after a stall")
