@@ -128,8 +128,10 @@ def test_multiquery_partition_slots_tiles_and_combine_ranges():
     rng = random.Random(1)
     for _ in range(1500):
         B, hkv = rng.randint(1, 6), rng.randint(1, 3)
-        G, RT = rng.choice([1, 2, 4]), rng.choice([16, 32, 64])
-        max_q = rng.randint(1, 20)
+        # tile heights of the 16-rows-per-warp kernel (16, 32, 64) and of the
+        # short-run kernels (8, 16 or 24 rows on the MMA's N side, one tile)
+        G, RT = rng.choice([1, 2, 4, 8]), rng.choice([8, 16, 24, 32, 64])
+        max_q = rng.randint(1, 20) if RT in (32, 64) or rng.random() < 0.5 else max(1, RT // G)
         ns = [rng.choice([0, 1, rng.randint(0, max_q)]) for _ in range(B)]
         Ls = [n + rng.randint(0, 90) for n in ns]
         tmax = -(-max_q * G // RT)
