@@ -111,11 +111,23 @@ def load_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+_CODE_TOKENS = re.compile(rb'("(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\')|/\*.*?\*/|//[^\n]*',
+                          re.S)
+
+
+def code_only(text: bytes) -> bytes:
+    """C++ source without its comments, whitespace runs collapsed to one
+    space: what the compiler sees, up to formatting."""
+    text = _CODE_TOKENS.sub(lambda m: m.group(1) if m.group(1) else b" ", text)
+    return re.sub(rb"\s+", b" ", text).strip()
+
+
 def kernel_source_hash(source="decode.cu") -> str:
     """sha256 (first 16 hex digits) of the device code a kernel is built from:
     each file of ``source`` (a name or a tuple of names) up to its host-code
-    marker line (``// ---- ... host ---``), followed by common.cuh. Host-side
-    edits below the marker leave it alone."""
+    marker line (``// ---- ... host ---``), followed by common.cuh, comments
+    and formatting left out (:func:`code_only`). Host-side edits below the
+    marker, and comment-only edits, leave it alone."""
     import hashlib
     csrc = os.path.join(ROOT, "paged_kv_decode_05_gb300", "csrc")
     text = b""
@@ -123,9 +135,9 @@ def kernel_source_hash(source="decode.cu") -> str:
         with open(os.path.join(csrc, name), "rb") as f:
             part = f.read()
         m = re.search(rb"^// -+ host -+$", part, re.M)
-        text += part[:m.start()] if m else part
+        text += code_only(part[:m.start()] if m else part) + b"\n"
     with open(os.path.join(csrc, "common.cuh"), "rb") as f:
-        text += f.read()
+        text += code_only(f.read())
     return hashlib.sha256(text).hexdigest()[:16]
 
 

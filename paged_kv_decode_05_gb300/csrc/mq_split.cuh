@@ -27,7 +27,9 @@
 //
 // This header holds the mma.sync split kernel and its combine; mq.cu
 // instantiates them for fp16 / bf16 caches (and holds the tcgen05 kernel for
-// long query runs), mq_i8.cu for INT8 caches, in parallel compilations.
+// long query runs), mq_i8.cu for INT8 caches, in parallel compilations. The
+// short-run kernels (query rows on the MMA's N side) live in mq_t.cu and use
+// the partition, prefix and combine defined here.
 #pragma once
 
 #include <cuda.h>

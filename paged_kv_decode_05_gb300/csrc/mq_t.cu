@@ -1,5 +1,6 @@
-// Multi-query attention over fp16 / bf16 caches for short query runs: at most
-// 24 rows (n_b queries x g heads) per (sequence, kv head), the shape of
+// Multi-query attention for short query runs, over fp16 / bf16 caches and
+// (head_dim 128) INT8 caches: at most 24 rows (n_b queries x g heads) per
+// (sequence, kv head), the shape of
 // speculative verification, where the target model scores the draft's
 // tokens plus one in one batched pass (Continuous-Batching-LLM-Inference-
 // Engine README, feature list "Speculative decoding"). Query i of sequence b

@@ -18,7 +18,13 @@ def _fake_tree(tmp_path, source="decode.cu", body=b"kernel v1"):
     (csrc / source).write_bytes(body)
     (csrc / "common.cuh").write_bytes(b"helpers")
     (tmp_path / "profiles").mkdir()
-    return csrc, hashlib.sha256(body + b"helpers").hexdigest()[:16]
+    return csrc, _hash(body)
+
+
+def _hash(*bodies):
+    """The expected hash: each source's code, then common.cuh's ("helpers")."""
+    text = b"".join(bench.code_only(b) + b"\n" for b in bodies) + bench.code_only(b"helpers")
+    return hashlib.sha256(text).hexdigest()[:16]
 
 
 def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
@@ -46,7 +52,7 @@ def test_traffic_record_ignores_host_code_below_the_marker(tmp_path, monkeypatch
     host = b"// ------------------------------------------------ host ---\nint f() { return 1; }\n"
     csrc, _ = _fake_tree(tmp_path, body=device + host)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    h = hashlib.sha256(device + b"helpers").hexdigest()[:16]
+    h = _hash(device)
     assert bench.kernel_source_hash("decode.cu") == h
     prof = tmp_path / "profiles" / "decode_split_kernel_gqa8b.md"
     prof.write_text(f"traffic_bytes_per_launch: 99 source_sha256: {h}\n")
@@ -54,6 +60,21 @@ def test_traffic_record_ignores_host_code_below_the_marker(tmp_path, monkeypatch
     (csrc / "decode.cu").write_bytes(device + host + b"int g() { return 2; }\n")
     assert bench.recorded_traffic("decode_split_kernel", "gqa8b") == 99
     (csrc / "decode.cu").write_bytes(b"__global__ void k2() {}\n" + host)
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") is None
+
+
+def test_traffic_record_ignores_comments_and_formatting(tmp_path, monkeypatch):
+    """A comment or a reformatting above the marker leaves the record current;
+    a change inside a string literal (e.g. inline PTX) does not."""
+    device = b'__global__ void k() { asm("mov.u32 %0, 1;"); }\n'
+    csrc, h = _fake_tree(tmp_path, body=device)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    prof = tmp_path / "profiles" / "decode_split_kernel_gqa8b.md"
+    prof.write_text(f"traffic_bytes_per_launch: 7 source_sha256: {h}\n")
+    (csrc / "decode.cu").write_bytes(b"// the kernel\n/* two\n lines */\n__global__ void k()\n{\n"
+                                     b'    asm("mov.u32 %0, 1;");   // one move\n}\n')
+    assert bench.recorded_traffic("decode_split_kernel", "gqa8b") == 7
+    (csrc / "decode.cu").write_bytes(b'__global__ void k() { asm("mov.u32 %0, 2;"); }\n')
     assert bench.recorded_traffic("decode_split_kernel", "gqa8b") is None
 
 
