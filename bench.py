@@ -122,6 +122,19 @@ def code_only(text: bytes) -> bytes:
     return re.sub(rb"\s+", b" ", text).strip()
 
 
+def mq_kernel_for(kv_dtype: str, head_dim: int, rows: int):
+    """The multi-query kernel pkv_multiquery_attn runs for ``rows`` = q_len x
+    group size (q and out 16-byte aligned), and the sources its device code
+    comes from: the library's dispatch rule, checked against the library's
+    own planner by tests/test_bench_host.py."""
+    i8 = kv_dtype == "i8"
+    if not i8 and rows >= 128:
+        return "mq_tc_kernel", ("mq_split.cuh", "mq.cu")
+    if rows <= 24 and (not i8 or head_dim == 128):
+        return ("mqt_i8_split_kernel" if i8 else "mqt_split_kernel"), ("mq_split.cuh", "mq_t.cu")
+    return "mq_split_kernel", ("mq_split.cuh",)
+
+
 def kernel_source_hash(source="decode.cu") -> str:
     """sha256 (first 16 hex digits) of the device code a kernel is built from:
     each file of ``source`` (a name or a tuple of names) up to its host-code
@@ -801,15 +814,7 @@ def run_multiquery(args):
     # runs the 16-rows-per-warp split kernel and the combine, two launches
     # each. Plus the append (two kernels for INT8).
     g = cfg.num_q_heads // cfg.num_kv_heads
-    rows = nq * g
-    i8 = cfg.kv_dtype == "i8"
-    if not i8 and rows >= 128:
-        kernel, src = "mq_tc_kernel", ("mq_split.cuh", "mq.cu")
-    elif rows <= 24 and (not i8 or cfg.head_dim == 128):
-        kernel = "mqt_i8_split_kernel" if i8 else "mqt_split_kernel"
-        src = ("mq_split.cuh", "mq_t.cu")
-    else:
-        kernel, src = "mq_split_kernel", ("mq_split.cuh",)
+    kernel, src = mq_kernel_for(cfg.kv_dtype, cfg.head_dim, nq * g)
     tc = kernel == "mq_tc_kernel"
     launches = (1 if tc else 2) + (2 if cfg.kv_dtype == "i8" else 1)
     traffic = recorded_traffic(kernel, args.config, src)

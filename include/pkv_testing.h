@@ -66,6 +66,22 @@ pkv_status pkv_testing_multiquery_attn_stall(const void *q, pkv_dtype q_dtype,
                                              int32_t stall_cta, uint32_t *dev_status,
                                              cudaStream_t stream);
 
+/* Which kernel pkv_multiquery_attn runs for these sizes (q and out taken as
+ * 16-byte aligned), and its row-tile height: PKV_TESTING_MQ_TCGEN05
+ * (128-row tiles, no split), PKV_TESTING_MQ_SHORT / PKV_TESTING_MQ_SHORT_I8
+ * (query rows on the MMA's N side, one warp per worker; fp16 / bf16 and
+ * INT8 caches), PKV_TESTING_MQ_ROWS16 (16 rows per warp, one CTA per
+ * worker). num_parts must be positive (no device query). Returns the size
+ * and argument checks of pkv_multiquery_workspace_size. */
+#define PKV_TESTING_MQ_TCGEN05 0
+#define PKV_TESTING_MQ_SHORT 1
+#define PKV_TESTING_MQ_SHORT_I8 2
+#define PKV_TESTING_MQ_ROWS16 3
+pkv_status pkv_testing_multiquery_kernel(int32_t batch, int32_t num_q_heads, int32_t max_q_len,
+                                         const pkv_cache_desc *cache, pkv_dtype q_dtype,
+                                         int32_t num_parts, int32_t *kernel,
+                                         int32_t *rows_per_tile);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,8 @@ _SIGS = {
                                                      _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
                                                      _SZ, _I32, ctypes.c_uint64, _I32,
                                                      _P, _P]),
+    "pkv_testing_multiquery_kernel": (ctypes.c_int, [_I32, _I32, _I32, _DESC, ctypes.c_int, _I32,
+                                                     _P, _P]),
     "pkv_testing_multiquery_attn_stall": (ctypes.c_int, [_P, ctypes.c_int, _P, _I32, _P, _P, _P,
                                                          _P, _DESC, _P, _I32, _P, _I32, _I32,
                                                          ctypes.c_float, _P, _P, _SZ, _I32,
@@ -311,3 +313,18 @@ def pkv_testing_multiquery_attn_stall(q, cu_q, max_q_len, k_cache, v_cache, bloc
         workspace.numel() * workspace.element_size(), int(num_parts), int(wait_limit_ns),
         int(stall_cta), _ptr(dev_status), _stream(stream))
     _check("pkv_testing_multiquery_attn_stall", code)
+
+
+MQ_KERNELS = {0: "mq_tc_kernel", 1: "mqt_split_kernel", 2: "mqt_i8_split_kernel",
+              3: "mq_split_kernel"}
+
+
+def pkv_testing_multiquery_kernel(batch, num_q_heads, max_q_len, desc, q_dtype, num_parts=16):
+    """Test hook: (kernel name, rows per tile) that pkv_multiquery_attn runs for
+    these sizes, from the library's own planner (no GPU needed)."""
+    kernel, rt = ctypes.c_int32(-1), ctypes.c_int32(0)
+    code = lib().pkv_testing_multiquery_kernel(int(batch), int(num_q_heads), int(max_q_len),
+                                               ctypes.byref(desc), int(q_dtype), int(num_parts),
+                                               ctypes.byref(kernel), ctypes.byref(rt))
+    _check("pkv_testing_multiquery_kernel", code)
+    return MQ_KERNELS[kernel.value], rt.value

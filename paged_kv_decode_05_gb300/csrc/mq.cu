@@ -683,6 +683,15 @@ namespace {
 
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
+// The tcgen05 launcher that serves runs of max_q rows per query head group
+// over this cache (16-bit caches, rows filling 128-row tiles), or nullptr;
+// q and out must also be 16-byte aligned.
+TcLaunch tc_for(const pkv_cache_desc* cache, int max_q, int G) {
+    if (cache->kv_dtype == PKV_I8 || (long long)max_q * G < kTcRows) return nullptr;
+    return cache->kv_dtype == PKV_BF16 ? tc_pick<BF16>(cache->head_dim, G)
+                                       : tc_pick<F16>(cache->head_dim, G);
+}
+
 pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
                           int32_t max_q_len, const void* k_cache, const void* v_cache,
                           const float* k_scales, const float* v_scales,
@@ -728,11 +737,8 @@ pkv_status run_multiquery(const void* q, pkv_dtype q_dtype, const int32_t* cu_q,
     // Query runs of 16-bit caches that fill 128-row tiles take the tcgen05
     // kernel (no split, no combine, no workspace); shorter runs, and every run
     // over an INT8 cache, the mma.sync kernel below.
-    const TcLaunch tc = (!i8 && (long long)max_q_len * pl.G >= kTcRows && mq_aligned(q, 16) &&
-                         mq_aligned(out, 16))
-                            ? (cache->kv_dtype == PKV_BF16 ? tc_pick<BF16>(cache->head_dim, pl.G)
-                                                           : tc_pick<F16>(cache->head_dim, pl.G))
-                            : nullptr;
+    const TcLaunch tc = mq_aligned(q, 16) && mq_aligned(out, 16)
+                            ? tc_for(cache, max_q_len, pl.G) : nullptr;
     if (tc) {
         MqParams p;
         p.q = q; p.cu_q = cu_q; p.block_tables = block_tables; p.context_lens = context_lens;
@@ -806,6 +812,26 @@ extern "C" pkv_status pkv_multiquery_attn(const void* q, pkv_dtype q_dtype, cons
 
 // ------------------------------------------------------------- test hook ---
 #include "../../include/pkv_testing.h"
+
+extern "C" pkv_status pkv_testing_multiquery_kernel(int32_t batch, int32_t num_q_heads,
+                                                    int32_t max_q_len, const pkv_cache_desc* cache,
+                                                    pkv_dtype q_dtype, int32_t num_parts,
+                                                    int32_t* kernel, int32_t* rows_per_tile) {
+    if (!kernel || !rows_per_tile || num_parts <= 0) return PKV_ERR_INVALID_ARG;
+    MqPlan pl;
+    const pkv_status s = mq_plan(cache, batch, num_q_heads, max_q_len, q_dtype, num_parts, &pl);
+    if (s != PKV_OK) return s;
+    if (tc_for(cache, max_q_len, pl.G)) {
+        *kernel = PKV_TESTING_MQ_TCGEN05;
+        *rows_per_tile = kTcRows;
+        return PKV_OK;
+    }
+    *kernel = pl.ops.src == kMqSrcI8Map ? PKV_TESTING_MQ_SHORT_I8
+              : pl.ops.wpc > 1          ? PKV_TESTING_MQ_SHORT
+                                        : PKV_TESTING_MQ_ROWS16;
+    *rows_per_tile = pl.ops.rt;
+    return PKV_OK;
+}
 
 extern "C" pkv_status pkv_testing_multiquery_attn_stall(
     const void* q, pkv_dtype q_dtype, const int32_t* cu_q, int32_t max_q_len, const void* k_cache,

@@ -221,3 +221,29 @@ def test_error_figures_of_the_test_helper():
     with pytest.raises(AssertionError):
         assert_attention_close(want + 3e-3, want, False)        # 3e-3 > 2e-3 + 1e-2 * 0
     assert assert_attention_close(want + 1e-2, want, True)[0] < 2e-2
+
+
+def test_multiquery_kernel_rule_matches_the_library():
+    """bench.py names the multi-query kernel in its roofline by a mirror of
+    the library's dispatch rule; the library's planner (a test hook, no GPU)
+    must pick the same kernel for every cache type, head dim, group size and
+    query count."""
+    from paged_kv_decode_05_gb300 import binding as B
+    from paged_kv_decode_05_gb300.build import build
+    build()
+    dt = {"bf16": B.PKV_BF16, "f16": B.PKV_F16, "i8": B.PKV_I8}
+    for kv in ("bf16", "f16", "i8"):
+        for d in (64, 128):
+            for g in (1, 2, 4, 8):
+                desc = B.CacheDesc(64, 16, 2, d, dt[kv])
+                for nq in (1, 2, 3, 5, 6, 7, 8, 9, 12, 16, 24, 25, 31, 32, 33, 64, 128):
+                    q_dtype = B.PKV_BF16 if kv == "i8" else dt[kv]
+                    name, rt = B.pkv_testing_multiquery_kernel(4, 2 * g, nq, desc, q_dtype)
+                    assert name == bench.mq_kernel_for(kv, d, nq * g)[0], (kv, d, g, nq)
+                    rows = nq * g
+                    if name == "mqt_split_kernel" or name == "mqt_i8_split_kernel":
+                        assert rt == 8 * -(-rows // 8) and rt <= 24
+                    elif name == "mq_tc_kernel":
+                        assert rt == 128
+                    else:
+                        assert rt in (16, 32, 64)
