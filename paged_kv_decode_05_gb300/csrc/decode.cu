@@ -80,7 +80,8 @@ struct Cfg {
     static constexpr int OFF_META = align_up(OFF_BAR + NS * 8, 16);   // int4 per stage
     static constexpr int OFF_SCL = OFF_META + NS * 16;                // float2 per stage, block
     static constexpr int OFF_P = align_up(OFF_SCL + NS * UB * 8, 16); // float4 reads
-    // P[head][token] rows in shared memory: UT floats each
+    // P[head][token] rows in shared memory: UT floats each (INT8: UT fp16
+    // values, the B operand's type, in the same space)
     static constexpr int PS = UT;
     // q rows of a piece's (sequence, kv head), copied with its first unit
     static constexpr int OFF_Q = align_up(OFF_P + PS * G * 4, 128);
@@ -801,18 +802,21 @@ decode_split_kernel(const DecodeParams p) {
                     const float p0 = (sv[bi][0][e] == -INFINITY) ? 0.f : fast_exp2(sv[bi][0][e] - mn);
                     const float p1 = (sv[bi][1][e] == -INFINITY) ? 0.f : fast_exp2(sv[bi][1][e] - mn);
                     ls = ls + p0 + p1;
-                    float w0 = p0, w1 = p1;   // the P.V weights as the MMA will take them
                     if constexpr (C::kI8) {
                         // P times the block's V scale, rounded to fp16 here, so that
-                        // the bias sum uses exactly the weights the MMA multiplies
-                        const float2 r = __half22float2(__floats2half2_rn(p0 * vsc[bi], p1 * vsc[bi]));
-                        w0 = r.x;
-                        w1 = r.y;
-                        wsum += w0 + w1;
-                    }
-                    if (2 * tq + e < G) {   // P[head][token]
-                        pbuf[(2 * tq + e) * C::PS + kBlockSize * bi + gq] = w0;
-                        pbuf[(2 * tq + e) * C::PS + kBlockSize * bi + gq + 8] = w1;
+                        // the bias sum uses exactly the weights the MMA multiplies;
+                        // stored as fp16, the B operand's own type
+                        const __half2 h = __floats2half2_rn(p0 * vsc[bi], p1 * vsc[bi]);
+                        const float2 r = __half22float2(h);
+                        wsum += r.x + r.y;
+                        if (2 * tq + e < G) {   // P[head][token]
+                            __half* ph16 = reinterpret_cast<__half*>(pbuf);
+                            ph16[(2 * tq + e) * C::PS + kBlockSize * bi + gq] = __low2half(h);
+                            ph16[(2 * tq + e) * C::PS + kBlockSize * bi + gq + 8] = __high2half(h);
+                        }
+                    } else if (2 * tq + e < G) {   // P[head][token]
+                        pbuf[(2 * tq + e) * C::PS + kBlockSize * bi + gq] = p0;
+                        pbuf[(2 * tq + e) * C::PS + kBlockSize * bi + gq + 8] = p1;
                     }
                 }
                 lsum[e] = ls;
@@ -842,10 +846,14 @@ decode_split_kernel(const DecodeParams p) {
                 if (gq < G) {
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        const float2 f = *reinterpret_cast<const float2*>(
-                            pbuf + gq * C::PS + kBlockSize * bi + 2 * tq + 8 * k);
-                        ph[k] = pack2<MMT>(f.x, f.y);
-                        if constexpr (!C::kI8) {
+                        if constexpr (C::kI8) {   // two fp16 weights, tokens 2tq + 8k, + 1
+                            ph[k] = *reinterpret_cast<const uint32_t*>(
+                                reinterpret_cast<const __half*>(pbuf) + gq * C::PS +
+                                kBlockSize * bi + 2 * tq + 8 * k);
+                        } else {
+                            const float2 f = *reinterpret_cast<const float2*>(
+                                pbuf + gq * C::PS + kBlockSize * bi + 2 * tq + 8 * k);
+                            ph[k] = pack2<MMT>(f.x, f.y);
                             const float2 r = unpack2(MMT{}, ph[k]);
                             pl[k] = pack2<MMT>(f.x - r.x, f.y - r.y);
                         }
