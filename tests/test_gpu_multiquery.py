@@ -55,9 +55,12 @@ SMALL = {
                          kv_dtype="f16", q_dtype="f16", src_dtype="f16", q_len=9,
                          len_groups=((6, 9, 500),)),
     "g4_q1": variant(CONFIGS["gqa8b"], batch=9, len_groups=((9, 1, 700),)),
-    # 7 queries x group 4 = 28 rows: the mma.sync kernel's 32-row tile (fewer
-    # than 25 rows take the short-run kernel, rows on the MMA's N side)
+    # 7 x 4 = 28, 9 x 4 = 36 and 4 x 8 = 32 rows: the 16-rows-per-warp kernel
+    # (24 rows or fewer take the short-run kernel, rows on the MMA's N side)
     "g4_q7": variant(CONFIGS["spec_verify"], batch=7, q_len=7, len_groups=((7, 7, 600),)),
+    "g4_q9": variant(CONFIGS["spec_verify"], batch=7, q_len=9, len_groups=((7, 9, 600),)),
+    "g8_q4_f16": variant(CONFIGS["gqa70b"], batch=5, q_len=4, kv_dtype="f16", q_dtype="f16",
+                         src_dtype="f16", len_groups=((5, 4, 700),)),
     "g2_q8_d64": variant(CONFIGS["gqa8b"], batch=6, num_q_heads=4, num_kv_heads=2, head_dim=64,
                          q_len=8, len_groups=((6, 8, 500),)),
     "g8_q3_f16": variant(CONFIGS["gqa70b"], batch=5, q_len=3, kv_dtype="f16", q_dtype="f16",

@@ -95,8 +95,10 @@ MQ = {
     # 5 queries x group 4 = 20 rows: the short-run split kernels (bf16, INT8)
     "spec_verify": variant(CONFIGS["spec_verify"], batch=6, len_groups=((6, 5, 600),)),
     "spec_verify_int8": variant(CONFIGS["spec_verify_int8"], batch=6, len_groups=((6, 5, 600),)),
-    # 7 queries x group 4 = 28 rows: the 16-rows-per-warp split kernel
+    # 7 x 4 = 28 and 10 x 4 = 40 rows: the 16-rows-per-warp split kernel (two
+    # and four consumer warps)
     "rows28": variant(CONFIGS["spec_verify"], batch=6, q_len=7, len_groups=((6, 7, 600),)),
+    "rows40": variant(CONFIGS["spec_verify"], batch=6, q_len=10, len_groups=((6, 10, 600),)),
     # 64 queries x group 4 = 256 rows: the tcgen05 kernel
     "prefill_chunk": variant(CONFIGS["prefill_chunk"], batch=2, q_len=64, max_len=500,
                              len_groups=((2, 64, 500),)),
