@@ -159,7 +159,8 @@ def test_peaks_measured_or_fallback(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.load_peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
     assert bench.load_tensor_peak() == (bench.FALLBACK_BF16_TFLOPS, "fallback")
-    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6794.8, "bf16_tflops": 1919.9}))
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        json.dumps({"hbm_gbs": 6794.8, "bf16_tflops": 1919.9}))
     assert bench.load_peaks() == (6794.8, "measured")
     assert bench.load_tensor_peak() == (1919.9, "measured")
 

@@ -4,7 +4,8 @@ import numpy as np
 import pytest
 
 import oracle
-from _pkv_helpers import GpuCase, OracleCase, assert_attention_close, out_to_f64, to_dev, to_host_bits
+from _pkv_helpers import (GpuCase, OracleCase, assert_attention_close, out_to_f64, to_dev,
+                          to_host_bits)
 from paged_kv_decode_05_gb300.workloads import CONFIGS, make_workload, variant
 
 pytestmark = pytest.mark.gpu

@@ -32,7 +32,9 @@ def test_graph_replay_equals_eager(name, mode):
                                                            len_groups=((20, 1, 1200),))
     w = make_workload(cfg)
     g = GpuCase(w, append_step=False)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()  # noqa: E731
+    def dev(a):
+        b = a.view(np.int16) if a.dtype == np.uint16 else a
+        return torch.from_numpy(np.ascontiguousarray(b)).cuda()
     k_step, v_step, slots = dev(w.k_step), dev(w.v_step), dev(w.step_slots)
     if w.k_step.dtype == np.uint16:
         k_step, v_step = k_step.view(torch.bfloat16), v_step.view(torch.bfloat16)

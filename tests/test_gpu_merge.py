@@ -50,7 +50,8 @@ def make_states(rows, heads, D, seed, max_pieces=6, empty_rows=(), score_std=3.0
                       for i in range(k)]
                 want[r, h] = oracle.merge_states(st)
                 want_m[r, h] = pm[:, h].max()
-                want_l[r, h] = sum(np.exp(np.float64(pm[i, h]) - want_m[r, h]) * np.float64(pl[i, h])
+                want_l[r, h] = sum(np.exp(np.float64(pm[i, h]) - want_m[r, h]) *
+                                   np.float64(pl[i, h])
                                    for i in range(k))
         m_l.append(pm); l_l.append(pl); o_l.append(po)
         ptr.append(ptr[-1] + k)

@@ -169,7 +169,8 @@ def test_first_prefill_chunk_from_position_zero(dtype, n):
     for parts in (0, 5):
         out = run_mq(g, w.q, w.cu_q, n, parts)
         _sync()
-        assert_attention_close(out_to_f64(out), want, dtype == "i8", f"{dtype} from 0 parts={parts}")
+        assert_attention_close(out_to_f64(out), want, dtype == "i8",
+                               f"{dtype} from 0 parts={parts}")
 
 
 # Query runs that fill 128-row tiles (q_len * g >= 128) take the tcgen05 kernel.
@@ -236,8 +237,9 @@ def test_bad_block_entry_and_length_are_flagged(name):
     qd = to_dev(w.q)
     out = torch.full(qd.shape, float("nan"), dtype=qd.dtype, device="cuda")
     cu = to_dev(np.asarray(w.cu_q, np.int32))
-    ws = torch.empty(B.pkv_multiquery_workspace_size(w.cfg.batch, w.cfg.num_q_heads, w.cfg.q_len,
-                                                     g.k_cache, 0), dtype=torch.uint8, device="cuda")
+    nbytes = B.pkv_multiquery_workspace_size(w.cfg.batch, w.cfg.num_q_heads, w.cfg.q_len,
+                                             g.k_cache, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     B.pkv_multiquery_attn(qd, cu, w.cfg.q_len, g.k_cache, g.v_cache, bt, lens,
                           w.cfg.softmax_scale, out, ws, 0, status)
     _sync()

@@ -4,7 +4,8 @@ pkv_decode_attn bit for bit (cache and output) and matches the oracle."""
 import numpy as np
 import pytest
 
-from _pkv_helpers import GpuCase, OracleCase, assert_attention_close, out_to_f64, to_dev, to_host_bits
+from _pkv_helpers import (GpuCase, OracleCase, assert_attention_close, out_to_f64, to_dev,
+                          to_host_bits)
 from paged_kv_decode_05_gb300.workloads import CONFIGS, make_workload, variant
 
 pytestmark = pytest.mark.gpu

@@ -217,7 +217,8 @@ def test_copy_blocks_round_trip_canaries_and_order():
         assert np.array_equal(k[d_], k0[s_]) and np.array_equal(v[d_], v0[s_])
         assert np.array_equal(ks[d_], ks0[s_]) and np.array_equal(vs[d_], vs0[s_])
     untouched = [b for b in range(NB) if b not in (8, 9, 10)]
-    assert np.array_equal(k[untouched], k0[untouched]) and np.array_equal(ks[untouched], ks0[untouched])
+    assert np.array_equal(k[untouched], k0[untouched])
+    assert np.array_equal(ks[untouched], ks0[untouched])
     # pairs apply in order: a chain 1 -> 2 -> 6 carries block 1 to block 6
     k1 = k.copy()
     copy_blocks(k, v, np.array([1, 2]), np.array([2, 6]))
